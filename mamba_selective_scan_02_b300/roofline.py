@@ -1,0 +1,36 @@
+"""Algorithmic byte and exponential counts for the roofline of each kernel.
+
+These are the minimum the method must move or evaluate, not what a kernel
+happens to move: the fused scan never writes the discretised (Ā, B̄) of shape
+(batch, L, D, N) nor any intermediate state [Mamba and selective state spaces,
+from first principles — "The hardware-aware scan"].
+"""
+
+
+def algorithmic_bytes_scan(batch: int, dim: int, dstate: int, seqlen: int, io_bytes: int,
+                           has_z: bool = True, has_h0: bool = False, has_hL: bool = True) -> int:
+    """Bytes the fused scan must move at minimum: u, delta (and z) read once and
+    y written once per (b, d, t); B and C read once per (b, t) (not per
+    channel); A, D and bias once; h0 / hL once per (b, d, n)."""
+    per_elem = (3 if has_z else 2) + 1
+    n = batch * dim * seqlen * per_elem * io_bytes
+    n += 2 * batch * dstate * seqlen * io_bytes
+    n += dim * dstate * 4 + 2 * dim * 4
+    n += batch * dim * dstate * 4 * (int(has_h0) + int(has_hL))
+    return n
+
+
+def algorithmic_bytes_step(batch: int, dim: int, dstate: int, io_bytes: int,
+                           has_z: bool = True) -> int:
+    """Bytes per decode token: the fp32 state read and written once, u, delta
+    (z) read and y written per (b, d), B and C read per (b, n), A, D, bias once."""
+    n = 2 * batch * dim * dstate * 4
+    n += batch * dim * ((3 if has_z else 2) + 1) * io_bytes
+    n += 2 * batch * dstate * io_bytes
+    n += dim * dstate * 4 + 2 * dim * 4
+    return n
+
+
+def exps_scan(batch: int, dim: int, dstate: int, seqlen: int) -> int:
+    """One exponential Ā = exp(Δ·A) per (b, d, n, t)."""
+    return batch * dim * dstate * seqlen

@@ -1,0 +1,142 @@
+"""ctypes wrapper around the fp64 C oracle (test infrastructure only).
+
+Every array crosses as a C-contiguous float64 numpy array; ``None`` stands for
+the NULL pointers the C side accepts (no gate, zero skip, zero bias, zero
+initial state).  The arithmetic lives entirely in ``ssm_oracle.c``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssm_oracle.c")
+_LIB = os.path.join(_HERE, "libssm_oracle.so")
+_lib = None
+
+_D = ctypes.POINTER(ctypes.c_double)
+_I64 = ctypes.c_int64
+
+
+def source_path() -> str:
+    return _SRC
+
+
+def build(src: str = _SRC, out: str = _LIB, force: bool = False) -> str:
+    """Compile the oracle with gcc (IEEE fp64, no fast-math).  Returns the .so path."""
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + ".tmp%d" % os.getpid()
+        subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, src, "-lm"],
+                       check=True)
+        os.replace(tmp, out)
+    return out
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) and return the ctypes library."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _bind(lib):
+    lib.oracle_scan.restype = ctypes.c_int
+    lib.oracle_scan.argtypes = [_I64, _I64, _I64, _I64,
+                                _D, _D, _D, _D, _D, _D, _D, _D,
+                                ctypes.c_int, ctypes.c_int, _D, _D, _D, _I64, _I64]
+    lib.oracle_step.restype = ctypes.c_int
+    lib.oracle_step.argtypes = [_I64, _I64, _I64,
+                                _D, _D, _D, _D, _D, _D, _D, _D, _D,
+                                ctypes.c_int, ctypes.c_int, _D]
+    return lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(_D)
+
+
+def scan(u, delta, A, B, C, Dskip=None, z=None, bias=None, h0=None,
+         delta_softplus=True, zoh=False, threads: int = 1, lib=None):
+    """Forward scan.  u, delta, z: (b, D, L); B, C: (b, N, L); A: (D, N);
+    Dskip, bias: (D,); h0: (b, D, N).  Returns (y (b, D, L), hL (b, D, N)) in fp64.
+
+    ``threads`` > 1 splits the independent (b, d) channels over host threads; each
+    thread runs the unchanged sequential oracle on its own channel range."""
+    lib = lib or load()
+    u, delta, z, B, C, A, Dskip, bias, h0 = map(_f64, (u, delta, z, B, C, A, Dskip, bias, h0))
+    b, dim, L = u.shape
+    N = A.shape[1]
+    assert delta.shape == u.shape and B.shape == (b, N, L) and C.shape == (b, N, L)
+    assert z is None or z.shape == u.shape
+    y = np.empty((b, dim, L), np.float64)
+    hL = np.empty((b, dim, N), np.float64)
+    nch = b * dim
+
+    def run(c0, c1):
+        rc = lib.oracle_scan(b, dim, N, L, _p(u), _p(delta), _p(z), _p(B), _p(C), _p(A),
+                             _p(Dskip), _p(bias), int(bool(delta_softplus)), int(bool(zoh)),
+                             _p(h0), _p(y), _p(hL), c0, c1)
+        if rc != 0:
+            raise RuntimeError("oracle_scan failed")
+
+    if threads <= 1 or nch < 2:
+        run(0, nch)
+    else:
+        bounds = np.linspace(0, nch, min(threads, nch) + 1).astype(np.int64)
+        with ThreadPoolExecutor(len(bounds) - 1) as ex:
+            list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])), range(len(bounds) - 1)))
+    return y, hL
+
+
+def scan_channels(channels, u, delta, A, B, C, Dskip=None, z=None, bias=None, h0=None,
+                  delta_softplus=True, zoh=False, lib=None):
+    """Oracle on a sample of (b, d) channels of a large problem.
+
+    ``channels`` is a list of (b, d).  Only those rows are widened to fp64, so the
+    inputs may be multi-GB torch/numpy arrays.  Returns lists of y rows (L,) and
+    final states (N,)."""
+    ys, hs = [], []
+    for (bi, di) in channels:
+        row = lambda t: None if t is None else t[bi:bi + 1, di:di + 1]
+        yc, hc = scan(row(u), row(delta), A[di:di + 1], B[bi:bi + 1], C[bi:bi + 1],
+                      Dskip=None if Dskip is None else Dskip[di:di + 1],
+                      z=row(z), bias=None if bias is None else bias[di:di + 1],
+                      h0=None if h0 is None else h0[bi:bi + 1, di:di + 1],
+                      delta_softplus=delta_softplus, zoh=zoh, lib=lib)
+        ys.append(yc[0, 0])
+        hs.append(hc[0, 0])
+    return ys, hs
+
+
+def step(state, u, delta, A, B, C, Dskip=None, z=None, bias=None,
+         delta_softplus=True, zoh=False, lib=None):
+    """One decode token.  state: (b, D, N) fp64, updated in place (a new fp64
+    array is returned if the input was not already a contiguous float64 numpy
+    array).  u, delta, z: (b, D); B, C: (b, N).  Returns (y (b, D), state)."""
+    lib = lib or load()
+    st = _f64(state)
+    u, delta, z, B, C, A, Dskip, bias = map(_f64, (u, delta, z, B, C, A, Dskip, bias))
+    b, dim, N = st.shape
+    assert u.shape == (b, dim) and B.shape == (b, N) and A.shape == (dim, N)
+    y = np.empty((b, dim), np.float64)
+    rc = lib.oracle_step(b, dim, N, _p(st), _p(u), _p(delta), _p(z), _p(B), _p(C), _p(A),
+                         _p(Dskip), _p(bias), int(bool(delta_softplus)), int(bool(zoh)), _p(y))
+    if rc != 0:
+        raise RuntimeError("oracle_step failed")
+    return y, st

@@ -1,0 +1,309 @@
+"""Pins that tie the fp64 oracle to what the pages and the mathematics fix.
+
+Each ``pin_*`` function takes a loaded oracle library (ctypes) and raises
+AssertionError when the oracle disagrees with an independently computed
+expectation.  The expectations never reuse the oracle's sequential loop: they
+come from printed values, the convolution view, the gated-RNN closed form,
+limits, or the explicit product form of the unrolled recurrence.
+
+tests/test_oracle_pins.py runs them on the real oracle; tests/test_oracle_mutants.py
+runs them on deliberately broken copies of it and requires each copy to fail
+at least one pin.
+"""
+
+from __future__ import annotations
+
+import os
+
+import numpy as np
+from scipy.special import expit
+
+from oracle import oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _softplus(x):
+    return np.logaddexp(0.0, x)
+
+
+def _silu(x):
+    return x * expit(x)
+
+
+def _close(got, want, rtol, atol=0.0, what=""):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    err = np.abs(got - want)
+    bound = atol + rtol * np.abs(want)
+    assert np.all(err <= bound), f"{what}: max err {err.max():.3e} (bound {bound.max():.3e})"
+
+
+def read_golden(name="worked_example.txt"):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *nums = line.split()
+            vals[key] = [float(x) for x in nums]
+    return vals
+
+
+# --------------------------------------------------------------------------
+# P1: the worked example printed on "State space models and Mamba" —
+# "A worked example".  a = 0.8 is Ā = exp(Δ·A) with A = ln(0.8)/Δ; b = 0.5 is
+# the first-order B̄ = Δ·B with B = 0.5/Δ; C = 1, D = 0, no gate.
+
+def pin_worked_example(lib):
+    g = read_golden()
+    a, bb, u = g["a"][0], g["b"][0], np.array(g["u"])
+    L = len(u)
+    for dt in (1.0, 2.0, 0.37):                       # Δ must cancel out of Ā and B̄
+        A = np.array([[np.log(a) / dt]])
+        B = np.full((1, 1, L), bb / dt)
+        C = np.ones((1, 1, L))
+        delta = np.full((1, 1, L), dt)
+        y, hL = orc.scan(u.reshape(1, 1, L), delta, A, B, C, delta_softplus=False, lib=lib)
+        _close(y[0, 0], g["y"], 1e-12, 1e-14, "worked example outputs")
+        _close(hL[0, 0], [g["y"][-1]], 1e-12, 1e-14, "worked example final state")
+        imp = np.zeros((1, 1, L))
+        imp[0, 0, 0] = 1.0
+        k, _ = orc.scan(imp, delta, A, B, C, delta_softplus=False, lib=lib)
+        _close(k[0, 0], g["kernel"], 1e-12, 1e-14, "worked example kernel")
+    # the page's convolution view of the third output: kernel · reversed input
+    third = sum(g["kernel"][lag] * u[2 - lag] for lag in range(3))
+    _close(third, g["y"][2], 1e-12, 0, "convolution view of the third output")
+
+
+# --------------------------------------------------------------------------
+# P2: with Δ, B and C fixed in time the recurrence is the causal convolution
+# y = u * K̄, K̄_k = C Ā^k B̄ (Mamba notes on erikxu.me — "State Space Models";
+# "State space models and Mamba" — "One system, two views", whose K_0 carries
+# the D term).  A nonzero initial state h_{-1} adds C Ā^{t+1} h_{-1}.
+
+def pin_lti_convolution(lib, seed=11):
+    rng = np.random.default_rng(seed)
+    b, dim, N, L = 2, 3, 4, 24
+    A = -rng.uniform(0.1, 2.0, (dim, N))
+    Braw = rng.normal(size=(b, N))
+    Craw = rng.normal(size=(b, N))
+    draw = rng.normal(size=(b, dim))
+    bias = rng.normal(size=dim)
+    Dsk = rng.normal(size=dim)
+    u = rng.normal(size=(b, dim, L))
+    z = rng.normal(size=(b, dim, L))
+    h0 = rng.normal(size=(b, dim, N))
+    B = np.repeat(Braw[:, :, None], L, axis=2)
+    C = np.repeat(Craw[:, :, None], L, axis=2)
+    delta = np.repeat(draw[:, :, None], L, axis=2)
+    for zoh in (False, True):
+        for use_h0 in (False, True):
+            y, _ = orc.scan(u, delta, A, B, C, Dskip=Dsk, z=z, bias=bias,
+                            h0=h0 if use_h0 else None, zoh=zoh, lib=lib)
+            want = np.zeros_like(u)
+            for bi in range(b):
+                for d in range(dim):
+                    dt = _softplus(draw[bi, d] + bias[d])
+                    abar = np.exp(dt * A[d])
+                    bbar = (np.expm1(dt * A[d]) / A[d] if zoh else dt) * Braw[bi]
+                    K = np.array([np.sum(Craw[bi] * abar ** k * bbar) for k in range(L)])
+                    K[0] += Dsk[d]                        # K_0 = D + C B̄
+                    for t in range(L):
+                        acc = sum(K[k] * u[bi, d, t - k] for k in range(t + 1))
+                        if use_h0:
+                            acc += np.sum(Craw[bi] * abar ** (t + 1) * h0[bi, d])
+                        want[bi, d, t] = acc * _silu(z[bi, d, t])
+            _close(y, want, 1e-10, 1e-12, f"LTI convolution (zoh={zoh}, h0={use_h0})")
+
+
+# --------------------------------------------------------------------------
+# P3: with N = 1, A = -1, B = 1 and Δ = softplus(z_t), exact zero-order hold
+# gives the gated RNN h_t = (1 - σ(z_t)) h_{t-1} + σ(z_t) x_t
+# (first-principles page — "Discretisation: zero-order hold"; fdeinterviews
+# summary: with N = 1 the model is a gated RNN).
+
+def pin_gated_rnn(lib, seed=12):
+    rng = np.random.default_rng(seed)
+    L = 40
+    zt = rng.normal(0, 2, L)
+    x = rng.normal(size=L)
+    for h_init in (0.0, 1.7):
+        y, hL = orc.scan(x.reshape(1, 1, L), zt.reshape(1, 1, L), np.array([[-1.0]]),
+                         np.ones((1, 1, L)), np.ones((1, 1, L)),
+                         h0=np.array([[[h_init]]]), delta_softplus=True, zoh=True, lib=lib)
+        h = h_init
+        want = []
+        for t in range(L):
+            g = expit(zt[t])
+            h = (1 - g) * h + g * x[t]
+            want.append(h)
+        _close(y[0, 0], want, 1e-12, 1e-14, "gated RNN")
+        _close(hL[0, 0], [want[-1]], 1e-12, 1e-14, "gated RNN state")
+
+
+# --------------------------------------------------------------------------
+# P4: the Δ limits (first-principles page — "Discretisation: zero-order hold";
+# fdeinterviews summary): Δ → 0 keeps the state, Δ → ∞ wipes it; with exact
+# ZOH, A = -1 and B = 1 the state becomes the current input; with the
+# first-order B̄ it becomes Δ·B·u.
+
+def pin_delta_limits(lib, seed=13):
+    rng = np.random.default_rng(seed)
+    b, dim, N, L = 1, 2, 5, 12
+    A = -np.arange(1, N + 1, dtype=np.float64)[None].repeat(dim, 0)
+    u = rng.normal(size=(b, dim, L))
+    z = rng.normal(size=(b, dim, L))
+    B = rng.normal(size=(b, N, L))
+    C = rng.normal(size=(b, N, L))
+    Dsk = rng.normal(size=dim)
+    h0 = rng.normal(size=(b, dim, N))
+    # Δ → 0: softplus(-40) ≈ 4e-18
+    y, hL = orc.scan(u, np.full((b, dim, L), -40.0), A, B, C, Dskip=Dsk, z=z, h0=h0, lib=lib)
+    _close(hL, h0, 1e-15, 1e-15, "Δ→0 keeps the state")
+    want = np.einsum("bnt,bdn->bdt", C, h0) + Dsk[None, :, None] * u
+    _close(y, want * _silu(z), 1e-14, 1e-15, "Δ→0 output reads the kept state")
+    # Δ → ∞: the previous state no longer matters
+    big = np.full((b, dim, L), 1e4)
+    y1, h1 = orc.scan(u, big, A, B, C, Dskip=Dsk, z=z, h0=h0, delta_softplus=False, lib=lib)
+    y2, h2 = orc.scan(u, big, A, B, C, Dskip=Dsk, z=z, h0=-3 * h0, delta_softplus=False, lib=lib)
+    assert np.array_equal(y1, y2) and np.array_equal(h1, h2), "Δ→∞ must forget the initial state"
+    _close(y1[..., 0], (np.einsum("bn,bn->b", C[..., 0], 1e4 * B[..., 0])[:, None] * u[..., 0]
+                        + Dsk[None] * u[..., 0]) * _silu(z[..., 0]), 1e-12, 1e-12,
+           "Δ→∞ first-order state is Δ·B·u")
+    # exact ZOH, A = -1, B = 1, C = 1: h_t = u_t
+    yz, hz = orc.scan(u[:, :1], big[:, :1], np.array([[-1.0]]), np.ones((1, 1, L)),
+                      np.ones((1, 1, L)), h0=np.array([[[5.0]]]), delta_softplus=False,
+                      zoh=True, lib=lib)
+    _close(yz[0, 0], u[0, 0], 1e-15, 0, "Δ→∞ ZOH state is the current input")
+
+
+# --------------------------------------------------------------------------
+# P5: from h_{-1} = 0 the first state is B̄ x_0 and the first output C B̄ x_0
+# (erikxu.me notes — "State Space Models"), plus the skip and the gate.
+
+def pin_first_output(lib, seed=14):
+    rng = np.random.default_rng(seed)
+    b, dim, N, L = 2, 3, 8, 5
+    A = -rng.uniform(0.2, 3, (dim, N))
+    u = rng.normal(size=(b, dim, L))
+    dr = rng.normal(size=(b, dim, L))
+    z = rng.normal(size=(b, dim, L))
+    B = rng.normal(size=(b, N, L))
+    C = rng.normal(size=(b, N, L))
+    Dsk = rng.normal(size=dim)
+    bias = rng.normal(size=dim)
+    y, _ = orc.scan(u, dr, A, B, C, Dskip=Dsk, z=z, bias=bias, lib=lib)
+    for bi in range(b):
+        for d in range(dim):
+            dt = _softplus(dr[bi, d, 0] + bias[d])
+            want = (np.dot(C[bi, :, 0], dt * B[bi, :, 0]) * u[bi, d, 0] + Dsk[d] * u[bi, d, 0])
+            _close(y[bi, d, 0], want * _silu(z[bi, d, 0]), 1e-13, 1e-15, "first output")
+
+
+# --------------------------------------------------------------------------
+# P6: the unrolled time-varying recurrence written as explicit products,
+# y_t = C_t·[Σ_{k≤t} (Π_{s=k+1..t} Ā_s) B̄_k u_k + (Π_{s≤t} Ā_s) h_{-1}] + D u_t
+# (the selective output of the first-principles page — "Selection", whose
+# display equation was lost; rebuilt from the recurrence), gated by silu(z).
+
+def pin_product_form(lib, seed=15):
+    rng = np.random.default_rng(seed)
+    b, dim, N, L = 2, 3, 6, 14
+    A = -rng.uniform(0.1, 2.5, (dim, N))
+    u = rng.normal(size=(b, dim, L))
+    dr = rng.normal(0, 0.8, (b, dim, L))
+    z = rng.normal(size=(b, dim, L))
+    B = rng.normal(size=(b, N, L))
+    C = rng.normal(size=(b, N, L))
+    Dsk = rng.normal(size=dim)
+    bias = rng.normal(0, 0.5, dim)
+    h0 = rng.normal(size=(b, dim, N))
+    for zoh in (False, True):
+        y, hL = orc.scan(u, dr, A, B, C, Dskip=Dsk, z=z, bias=bias, h0=h0, zoh=zoh, lib=lib)
+        wy = np.zeros_like(u)
+        wh = np.zeros_like(h0)
+        for bi in range(b):
+            for d in range(dim):
+                dt = _softplus(dr[bi, d] + bias[d])                      # (L,)
+                abar = np.exp(dt[:, None] * A[d][None, :])               # (L, N)
+                if zoh:
+                    bbar = np.expm1(dt[:, None] * A[d][None, :]) / A[d][None, :] * B[bi].T
+                else:
+                    bbar = dt[:, None] * B[bi].T                         # (L, N)
+                for t in range(L):
+                    state = np.prod(abar[:t + 1], axis=0) * h0[bi, d]
+                    for k in range(t + 1):
+                        state = state + np.prod(abar[k + 1:t + 1], axis=0) * bbar[k] * u[bi, d, k]
+                    wy[bi, d, t] = (np.dot(C[bi, :, t], state) + Dsk[d] * u[bi, d, t]) * _silu(z[bi, d, t])
+                    if t == L - 1:
+                        wh[bi, d] = state
+        _close(y, wy, 1e-11, 1e-13, f"product form outputs (zoh={zoh})")
+        _close(hL, wh, 1e-11, 1e-13, f"product form final state (zoh={zoh})")
+
+
+# --------------------------------------------------------------------------
+# P7: the scan is a composition of affine maps h ↦ Ā h + B̄ u, associative
+# (erikxu.me notes — "Mamba"; first-principles page — "The hardware-aware
+# scan"), so a scan split at any token and resumed from the carried state
+# equals the whole scan; and a scan of length L equals L single-token decode
+# steps on a carried state.
+
+def pin_continuation(lib, seed=16):
+    rng = np.random.default_rng(seed)
+    b, dim, N, L = 2, 4, 5, 33
+    A = -rng.uniform(0.1, 2.0, (dim, N))
+    u = rng.normal(size=(b, dim, L))
+    dr = rng.normal(size=(b, dim, L))
+    z = rng.normal(size=(b, dim, L))
+    B = rng.normal(size=(b, N, L))
+    C = rng.normal(size=(b, N, L))
+    Dsk = rng.normal(size=dim)
+    bias = rng.normal(size=dim)
+    h0 = rng.normal(size=(b, dim, N))
+    kw = dict(Dskip=Dsk, bias=bias, lib=lib)
+    y, hL = orc.scan(u, dr, A, B, C, z=z, h0=h0, **kw)
+    for cut in (1, 13, 32):
+        ya, ha = orc.scan(u[..., :cut], dr[..., :cut], A, B[..., :cut], C[..., :cut],
+                          z=z[..., :cut], h0=h0, **kw)
+        yb, hb = orc.scan(u[..., cut:], dr[..., cut:], A, B[..., cut:], C[..., cut:],
+                          z=z[..., cut:], h0=ha, **kw)
+        _close(np.concatenate([ya, yb], -1), y, 1e-14, 1e-15, f"split at {cut}")
+        _close(hb, hL, 1e-14, 1e-15, f"state after split at {cut}")
+    # the same composition in pairs (a, b) ↦ (a2 a1, a2 b1 + b2), one channel
+    bi, d = 1, 2
+    dt = _softplus(dr[bi, d] + bias[d])
+    a = np.exp(dt[:, None] * A[d][None])
+    bb = dt[:, None] * B[bi].T * u[bi, d][:, None]
+    P, S = np.ones(N), np.zeros(N)
+    for t in range(L):
+        P, S = a[t] * P, a[t] * S + bb[t]
+    _close(hL[bi, d], P * h0[bi, d] + S, 1e-12, 1e-14, "affine-pair composition")
+
+
+def pin_decode_equals_scan(lib, seed=17):
+    rng = np.random.default_rng(seed)
+    b, dim, N, T = 3, 4, 6, 20
+    A = -rng.uniform(0.1, 2.0, (dim, N))
+    u = rng.normal(size=(b, dim, T))
+    dr = rng.normal(size=(b, dim, T))
+    z = rng.normal(size=(b, dim, T))
+    B = rng.normal(size=(b, N, T))
+    C = rng.normal(size=(b, N, T))
+    Dsk = rng.normal(size=dim)
+    bias = rng.normal(size=dim)
+    h0 = rng.normal(size=(b, dim, N))
+    for zoh in (False, True):
+        y, hL = orc.scan(u, dr, A, B, C, Dskip=Dsk, z=z, bias=bias, h0=h0, zoh=zoh, lib=lib)
+        st = h0.copy()
+        for t in range(T):
+            yt, st = orc.step(st, u[..., t], dr[..., t], A, B[..., t], C[..., t], Dskip=Dsk,
+                              z=z[..., t], bias=bias, zoh=zoh, lib=lib)
+            _close(yt, y[..., t], 1e-13, 1e-15, f"decode token {t} (zoh={zoh})")
+        _close(st, hL, 1e-13, 1e-15, f"decode carried state (zoh={zoh})")
+
+
+ALL_PINS = [pin_worked_example, pin_lti_convolution, pin_gated_rnn, pin_delta_limits,
+            pin_first_output, pin_product_form, pin_continuation, pin_decode_equals_scan]

@@ -1,0 +1,74 @@
+"""Planted mistakes in copies of the oracle must each fail at least one pin.
+
+Every mutant is a one-spot textual change to ``oracle/ssm_oracle.c`` of the
+kind a careless rewrite makes (a dropped term, a wrong sign, a wrong index, a
+transposed operand, an update out of order).  The copy is compiled into a
+temporary library on the CPU; the real oracle is never touched.
+"""
+
+import os
+
+import pytest
+
+import pins
+from oracle import oracle as orc
+
+MUTANTS = {
+    "drop_skip_term": ("double out = s + skip * u_c[t];", "double out = s;"),
+    "exp_sign": ("const double abar = exp(dt * A_d[n]);", "const double abar = exp(-dt * A_d[n]);"),
+    "read_before_update": (
+        "h[n] = abar * h[n] + bbar * u_c[t];\n                s += C_b[n * seqlen + t] * h[n];",
+        "s += C_b[n * seqlen + t] * h[n];\n                h[n] = abar * h[n] + bbar * u_c[t];"),
+    "B_transposed": ("oracle_bbar(dt, A_d[n], B_b[n * seqlen + t], zoh)",
+                     "oracle_bbar(dt, A_d[n], B_b[t * dstate + n], zoh)"),
+    "B_C_swapped": ("s += C_b[n * seqlen + t] * h[n];", "s += B_b[n * seqlen + t] * h[n];"),
+    "softplus_drops_x": ("return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));",
+                         "return x > 0.0 ? log1p(exp(-x)) : log1p(exp(x));"),
+    "bias_not_added": ("double dt = dt_c[t] + bias_d;", "double dt = dt_c[t];"),
+    "first_order_drops_delta": ("return delta * b;\n    return expm1", "return b;\n    return expm1"),
+    "zoh_missing_division": ("return expm1(delta * a) / a * b;", "return expm1(delta * a) * b;"),
+    "gate_is_sigmoid": ("return x / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(-x));"),
+    "h0_ignored": ("h[n] = h0 ? h0[c * dstate + n] : 0.0;", "h[n] = 0.0;"),
+    "A_row_of_channel_0": ("const double *A_d = A + d * dstate;", "const double *A_d = A;"),
+    "skip_of_channel_0": ("const double skip = Dskip ? Dskip[d] : 0.0;",
+                          "const double skip = Dskip ? Dskip[0] : 0.0;"),
+    "B_of_batch_0": ("const double *B_b = B + b * dstate * seqlen;", "const double *B_b = B;"),
+    "gate_only_on_state_term": (
+        "double out = s + skip * u_c[t];\n            if (z_c)\n                out *= oracle_silu(z_c[t]);",
+        "double out = s;\n            if (z_c)\n                out *= oracle_silu(z_c[t]);\n            out += skip * u_c[t];"),
+    "step_state_not_decayed": ("*h = abar * *h + bbar * u[c];", "*h = *h + bbar * u[c];"),
+    "step_B_of_batch_0": ("oracle_bbar(dt, a, B[b * dstate + n], zoh)", "oracle_bbar(dt, a, B[n], zoh)"),
+    "step_no_bias": ("double dt = delta[c] + (bias ? bias[d] : 0.0);", "double dt = delta[c];"),
+}
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(orc.source_path()) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, source, tmp_path):
+    old, new = MUTANTS[name]
+    assert source.count(old) == 1, f"mutant {name}: anchor not found exactly once"
+    src = tmp_path / f"{name}.c"
+    src.write_text(source.replace(old, new))
+    so = orc.build(str(src), str(tmp_path / f"lib{name}.so"), force=True)
+    lib = orc.load(so)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"planted mistake {name} passed every pin"
+
+
+def test_unmutated_copy_passes(source, tmp_path):
+    src = tmp_path / "same.c"
+    src.write_text(source)
+    lib = orc.load(orc.build(str(src), str(tmp_path / "libsame.so"), force=True))
+    for pin in pins.ALL_PINS:
+        pin(lib)
+    assert os.path.exists(str(tmp_path / "libsame.so"))
