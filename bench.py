@@ -1,0 +1,374 @@
+#!/usr/bin/env python
+"""Benchmark of the fused selective scan (and the decode step) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one forward selective scan over the Mamba-2.8B-shaped layer
+(batch 4, 5,120 channels, N = 16, L = 2,048, bf16 I/O, fp32 state), inputs
+resident in HBM.  Under torchrun every rank scans its own copy of the layer
+(channels are independent: no data-path collective, weak scaling); rank 0
+prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on the
+host cores on a bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan Gelem/s (batch·D·L) and HBM GB/s, % of min(HBM,MUFU) roofline"
+UNIT = "Gelem/s"
+WORKLOAD = "mamba2.8b_layer_L2048"
+DECODE = "decode_b256_64tok"
+HBM_FALLBACK_GBS = 6400.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "MEASURED_PEAKS.json (copy, measured)"
+    return HBM_FALLBACK_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Polls SM clock and clock-event reasons through NVML (read-only) in a thread."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_index: int, period_s: float = 0.02):
+        self.samples, self.period, self.ok = [], period_s, False
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            import torch
+            pynvml.nvmlInit()
+            uuid = str(torch.cuda.get_device_properties(torch_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.nv = pynvml
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # pragma: no cover - reported in the JSON
+            self.err = repr(e)
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append((mhz, reasons))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self.ok:
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": getattr(self, "err", "no samples")}
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(v for k, v in self.REASONS.items() if mask & k),
+                "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_rate(w, seconds: float, cores: int, seed_offset: int = 0):
+    """Gelem/s of the fp64 oracle on a bounded sample of ``w``'s channels: the
+    unchanged sequential oracle, its independent channels split over host threads."""
+    from mamba_selective_scan_02_b300.inputs import make_inputs
+    from oracle import oracle as orc
+
+    probe = make_inputs(w, batch=1, dim=max(1, cores), seed=w.seed + 1000 + seed_offset)
+    t0 = time.perf_counter()
+    orc.scan(probe["u"], probe["delta"], probe["A"], probe["B"], probe["C"], Dskip=probe["Dskip"],
+             z=probe["z"], bias=probe["bias"], threads=cores)
+    per_round = max(time.perf_counter() - t0, 1e-3)        # one channel per core
+    rounds = max(1, int(seconds / per_round))
+    dim = min(w.dim, cores * rounds)
+    inp = make_inputs(w, batch=1, dim=dim, seed=w.seed + 2000 + seed_offset)
+    t0 = time.perf_counter()
+    orc.scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], Dskip=inp["Dskip"], z=inp["z"],
+             bias=inp["bias"], threads=cores)
+    dt = time.perf_counter() - t0
+    elems = dim * w.seqlen
+    return elems / dt / 1e9, dt, f"{dim} channels x {w.seqlen} tokens (N={w.dstate}) of {w.name}"
+
+
+def run_reference(args):
+    from mamba_selective_scan_02_b300.inputs import WORKLOADS
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = WORKLOADS[WORKLOAD]
+    cores = os.cpu_count() or 1
+    per_step = max(0.5, 90.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup):
+        oracle_rate(w, per_step, cores, seed_offset=i)
+    rates, secs = [], 0.0
+    sample = ""
+    for i in range(args.steps):
+        r, dt, sample = oracle_rate(w, per_step, cores, seed_offset=100 + i)
+        rates.append(r)
+        secs += dt
+    value = statistics.median(rates)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
+                   "seqlen": w.seqlen, "io_dtype": w.io_dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample + " per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ GPU path
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from mamba_selective_scan_02_b300 import api, capi
+    from mamba_selective_scan_02_b300.inputs import WORKLOADS, make_inputs
+    from mamba_selective_scan_02_b300.roofline import (algorithmic_bytes_scan,
+                                                        algorithmic_bytes_step, exps_scan)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def allmax(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    w = WORKLOADS[WORKLOAD]
+    inp = make_inputs(w, device=dev)
+    y = torch.empty_like(inp["u"])
+    hL = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device=dev)
+    ws = torch.empty(api.workspace_bytes(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"]),
+                     dtype=torch.uint8, device=dev)
+    p = api.scan_params(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["Dskip"], inp["z"],
+                        inp["bias"], None, y=y, hL=hL, workspace=ws)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    launches_per_step = 1 if ws.numel() <= 256 else 3   # one chunk: a single kernel
+
+    # MUFU ex2 peak, measured on this GPU (the roofline's exponential side)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.empty(sms * 8 * 256, dtype=torch.float32, device=dev)
+    iters = 2048
+    ex2_count = sms * 8 * 256 * iters * 16
+    best = math.inf
+    for i in range(8):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        capi.check(capi.ssm_bench_mufu_ex2(sink.data_ptr(), sms * 8, iters, sh), "mufu bench")
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            best = min(best, e0.elapsed_time(e1))
+    mufu_peak = ex2_count / (best / 1e3) / 1e9  # G ex2/s
+
+    elems = w.batch * w.dim * w.seqlen
+    alg_bytes = algorithmic_bytes_scan(w.batch, w.dim, w.dstate, w.seqlen, 2)
+    exps = exps_scan(w.batch, w.dim, w.dstate, w.seqlen)
+    hbm_peak, hbm_src = measured_peaks()
+
+    for _ in range(max(3, args.warmup)):
+        capi.check(capi.ssm_scan_fwd(p, sh), "ssm_scan_fwd")
+    torch.cuda.synchronize(dev)
+    capi.check(api.workspace_status(ws), "scan status")
+
+    clocks = ClockSampler(local)
+    with clocks:
+        # keep warming until clocks settle (>= 0.5 s of load), then time exactly K steps
+        t_end = time.perf_counter() + 0.5
+        while time.perf_counter() < t_end:
+            for _ in range(50):
+                capi.ssm_scan_fwd(p, sh)
+            torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        ev[0].record(stream)
+        for i in range(args.steps):
+            capi.ssm_scan_fwd(p, sh)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    capi.check(api.workspace_status(ws), "scan status")
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    total_ms_max = allmax(total_ms)
+    ms_step = total_ms_max / args.steps
+    value = elems * args.steps * world / (total_ms_max / 1e3) / 1e9
+    kern_ms = statistics.mean(per_step)
+    achieved_ex2 = exps / (kern_ms / 1e3) / 1e9
+    achieved_gbs = alg_bytes / (kern_ms / 1e3) / 1e9
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
+                   "seqlen": w.seqlen, "io_dtype": w.io_dtype, "state_dtype": "f32",
+                   "parallelism": f"replicas x{world} (independent channels)",
+                   "l2": f"inputs larger than L2 ({alg_bytes / 1e6:.1f} MB per step)"},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {
+            "bound": "alu", "unit": "Gex2/s", "achieved": achieved_ex2, "peak": mufu_peak,
+            "frac": achieved_ex2 / mufu_peak, "traffic": None,
+            "peak_source": "MUFU ex2.approx throughput measured in this run (ssm_bench_mufu_ex2)",
+            "kernel_ms": kern_ms,
+            "hbm": {"achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved_gbs / hbm_peak, "peak_source": hbm_src,
+                    "algorithmic_bytes": alg_bytes},
+            "roofline_gelem_s": min(mufu_peak / w.dstate, hbm_peak / (alg_bytes / elems)),
+        },
+        "clocks": clocks.summary(),
+    }
+
+    # ---- end to end through the C ABI from pinned host buffers
+    if not args.no_e2e:
+        names = ("u", "delta", "z", "B", "C")
+        small = ("A", "Dskip", "bias")
+        host = {k: inp[k].cpu().pin_memory() for k in names + small}
+        dbuf = {k: torch.empty_like(inp[k]) for k in names + small}
+        hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        hh = torch.empty(hL.shape, dtype=hL.dtype).pin_memory()
+        pe = api.scan_params(dbuf["u"], dbuf["delta"], dbuf["A"], dbuf["B"], dbuf["C"], dbuf["Dskip"],
+                             dbuf["z"], dbuf["bias"], None, y=y, hL=hL, workspace=ws)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = hy.numel() * hy.element_size() + hh.numel() * hh.element_size()
+
+        def e2e_step():
+            for k, t in host.items():
+                dbuf[k].copy_(t, non_blocking=True)
+            capi.ssm_scan_fwd(pe, sh)
+            hy.copy_(y, non_blocking=True)
+            hh.copy_(hL, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        ksteps = max(3, min(args.steps, 50))
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ksteps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        ms = allmax(e0.elapsed_time(e1))
+        out["e2e"] = {"value": elems * ksteps * world / (ms / 1e3) / 1e9, "unit": UNIT,
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ksteps,
+                      "ms_per_step": ms / ksteps}
+        out["gpu_launches"] += launches_per_step * ksteps
+        del host, dbuf
+
+    # ---- decode: 64 consecutive tokens, L2 flushed before each (cold state as in a deep stack)
+    if not args.no_decode:
+        wd = WORKLOADS[DECODE]
+        dinp = make_inputs(wd, device=dev)
+        state = dinp["h0"].clone()
+        ydec = torch.empty((wd.batch, wd.dim), dtype=dinp["u"].dtype, device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        tok = [api.step_params(state, dinp["u"][t], dinp["delta"][t], dinp["A"], dinp["B"][t], dinp["C"][t],
+                               dinp["Dskip"], dinp["z"][t], dinp["bias"], y=ydec) for t in range(wd.seqlen)]
+        for t in range(4):
+            capi.check(capi.ssm_state_update(tok[t], sh), "ssm_state_update")
+        state.copy_(dinp["h0"])
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(wd.seqlen)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(wd.seqlen)]
+        for t in range(wd.seqlen):
+            flush.zero_()
+            starts[t].record(stream)
+            capi.ssm_state_update(tok[t], sh)
+            ends[t].record(stream)
+        torch.cuda.synchronize(dev)
+        tms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        dbytes = algorithmic_bytes_step(wd.batch, wd.dim, wd.dstate, 2)
+        mean_ms = statistics.mean(tms)
+        gbs = dbytes / (mean_ms / 1e3) / 1e9
+        out["decode"] = {"workload": wd.name, "tokens": wd.seqlen, "ms_per_token": mean_ms,
+                         "value": wd.batch * wd.dim / (mean_ms / 1e3) / 1e9, "unit": UNIT,
+                         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                                      "frac": gbs / hbm_peak, "traffic": None,
+                                      "algorithmic_bytes": dbytes},
+                         "l2": "256 MB written before every token; state 83.9 MB"}
+        out["gpu_launches"] += wd.seqlen + 4
+
+    # ---- CPU baseline: the fp64 oracle on a bounded sample (rank 0 only)
+    if rank == 0 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        r, dt, sample = oracle_rate(w, 15.0, cores)
+        out["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": sample, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

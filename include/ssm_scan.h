@@ -1,0 +1,143 @@
+/*
+ * ssm_scan.h — C ABI of libssmscan, the B300 (sm_103a) Mamba selective scan.
+ *
+ * Operation (forward scan), per batch b, channel d, state n and token t:
+ *
+ *   Δ_t     = softplus(Δraw[b,d,t] + bias[d])   (or Δraw + bias, see delta_softplus)
+ *   Ā_t,n   = exp(Δ_t · A[d,n])
+ *   B̄_t,n   = Δ_t · B[b,n,t]                    (first order; zoh = 1 selects the
+ *                                                 exact zero-order hold (Ā−1)/A · B)
+ *   h_t,n   = Ā_t,n · h_{t−1},n + B̄_t,n · u[b,d,t],   h_{−1} = h0 (zeros if NULL)
+ *   y[b,d,t]= (Σ_n C[b,n,t] · h_t,n + Dskip[d] · u[b,d,t]) · silu(z[b,d,t])
+ *   hL[b,d,n] = h_{L−1},n
+ *
+ * Sources: the SSM, its zero-order-hold discretisation and the first-order
+ * B̄ = ΔB — "Mamba and selective state spaces, from first principles",
+ * sections "A state space model", "Discretisation: zero-order hold"; the
+ * input-dependent Δ = softplus(bias + ·), B_t, C_t — same page, "Selection:
+ * B, C and Δ from the token"; the D·u skip — "State space models and Mamba",
+ * "One system, two views"; the silu gate branch — first-principles page,
+ * "The Mamba block"; the fused scan that writes only y — first-principles page,
+ * "The hardware-aware scan".
+ *
+ * The decode step (ssm_state_update) is the same recurrence with L = 1 on a
+ * carried state ("A fixed state against a growing cache", first-principles
+ * page; streaming inference in "One system, two views").
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, row-major and contiguous, with
+ *     the shapes given below.  The caller owns all memory; the library
+ *     allocates nothing (no cudaMalloc, no host allocation per call).
+ *   - Work is enqueued asynchronously on `stream` (0 = legacy default stream).
+ *   - Invalid arguments return SSM_ERR_INVALID_ARG / SSM_ERR_UNSUPPORTED and
+ *     launch nothing.  A failed launch returns SSM_ERR_CUDA.  Errors detected
+ *     on the device (a bounded wait that ran out) are recorded in the
+ *     workspace and read back by ssm_workspace_status.
+ *   - ssm_scan_fwd: u, delta, z, B, C, y, h0, hL and workspace must be
+ *     16-byte aligned; A, Dskip and delta_bias 4-byte aligned.
+ *     ssm_state_update: every pointer aligned to its element size.
+ *     y must not overlap any input.  hL may be the same buffer as h0.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ssm_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, small workspace */
+    SSM_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement (e.g. dstate > 16) */
+    SSM_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    SSM_ERR_TIMEOUT = 4      /* a device-side bounded wait ran out (reported via the workspace) */
+} ssm_status;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+/* Largest state size N the kernels are built for. */
+#define SSM_MAX_DSTATE 16
+
+typedef struct {
+    int64_t batch;          /* b  >= 1 */
+    int64_t dim;            /* D  >= 1 (channels) */
+    int64_t dstate;         /* N  in [1, SSM_MAX_DSTATE] */
+    int64_t seqlen;         /* L  >= 1 */
+    ssm_dtype io_dtype;     /* dtype of u, delta, z, B, C and y */
+    const void *u;          /* b × D × L, io_dtype */
+    const void *delta;      /* b × D × L, io_dtype: Δraw before bias / softplus */
+    const void *z;          /* b × D × L, io_dtype; NULL = no gate (factor 1) */
+    const void *B;          /* b × N × L, io_dtype */
+    const void *C;          /* b × N × L, io_dtype */
+    const float *A;         /* D × N fp32, any values (S4D-Real init is −(n+1)) */
+    const float *Dskip;     /* D fp32; NULL = 0 */
+    const float *delta_bias;/* D fp32; NULL = 0 */
+    int delta_softplus;     /* 1: Δ = softplus(Δraw + bias); 0: Δ = Δraw + bias */
+    int zoh;                /* 0: B̄ = Δ·B (first order); 1: exact ZOH (Ā − 1)/A · B */
+    const float *h0;        /* b × D × N fp32 initial state; NULL = zeros */
+    void *y;                /* out: b × D × L, io_dtype */
+    float *hL;              /* out: b × D × N fp32 final state; NULL = not written */
+    void *workspace;        /* device scratch of >= ssm_scan_workspace_size(...) bytes */
+    size_t workspace_bytes;
+    int64_t chunk_len;      /* 0 = automatic.  Otherwise the sequence is cut into
+                               chunks of this many tokens (a multiple of 64) that
+                               run in parallel and are joined by carried states. */
+} ssm_scan_params;
+
+/* Bytes of workspace ssm_scan_fwd needs for these sizes and chunk_len (never 0:
+ * the workspace always holds the device status word).  Returns 0 only when the
+ * sizes are invalid. */
+size_t ssm_scan_workspace_size(const ssm_scan_params *p);
+
+/* Forward selective scan: writes y and (if non-NULL) hL.  Also clears the
+ * workspace status word before launching. */
+ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream);
+
+typedef struct {
+    int64_t batch;          /* b >= 1 (independent sequences) */
+    int64_t dim;            /* D >= 1 */
+    int64_t dstate;         /* N in [1, SSM_MAX_DSTATE] */
+    ssm_dtype io_dtype;     /* dtype of u, delta, z, B, C and y */
+    float *state;           /* b × D × N fp32 carried state, read and updated in place */
+    const void *u;          /* b × D, io_dtype: this token's input */
+    const void *delta;      /* b × D, io_dtype */
+    const void *z;          /* b × D, io_dtype; NULL = no gate */
+    const void *B;          /* b × N, io_dtype */
+    const void *C;          /* b × N, io_dtype */
+    const float *A;         /* D × N fp32 */
+    const float *Dskip;     /* D fp32; NULL = 0 */
+    const float *delta_bias;/* D fp32; NULL = 0 */
+    int delta_softplus;
+    int zoh;
+    void *y;                /* out: b × D, io_dtype */
+} ssm_step_params;
+
+/* One decode token for every (b, d): the recurrence with L = 1 on `state`. */
+ssm_status ssm_state_update(const ssm_step_params *p, ssm_stream_t stream);
+
+/* Synchronises `stream`, then returns SSM_OK or the error a kernel recorded in
+ * this workspace (SSM_ERR_TIMEOUT), or SSM_ERR_CUDA if the copy fails. */
+ssm_status ssm_workspace_status(const void *workspace, ssm_stream_t stream);
+
+/* Static description of a status code. */
+const char *ssm_status_string(ssm_status s);
+
+/* Measurement helper (not part of the method): launches `blocks` × 256 threads
+ * that each evaluate 16 × iters dependent-free ex2.approx.ftz.f32 chains and
+ * write one float per thread to `sink` (blocks × 256 floats).  Timing it gives
+ * the MUFU ex2 throughput the scan's roofline is taken against. */
+ssm_status ssm_bench_mufu_ex2(float *sink, int blocks, int iters, ssm_stream_t stream);
+
+/* Library build identification, e.g. "libssmscan sm_103a". */
+const char *ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

@@ -1,0 +1,149 @@
+"""Torch-facing binding of libssmscan: argument marshalling only.
+
+Every step of the scan runs in the CUDA library; these functions check tensor
+placement, fill the C parameter structs with device pointers and the current
+stream, and allocate outputs and the workspace with torch when the caller does
+not pass them.  They raise if the library cannot be loaded — there is no CPU
+or PyTorch fallback.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import capi
+
+_DT = {torch.float32: capi.SSM_F32, torch.bfloat16: capi.SSM_BF16}
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, name, shape, dtype, device):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _opt(t, *args):
+    if t is not None:
+        _need(t, *args)
+
+
+def scan_params(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None, *, y, hL=None,
+                delta_softplus=True, zoh=False, chunk_len=0, workspace=None) -> capi.ScanParams:
+    """Validate tensors and build the C parameter struct (workspace may be None to size it)."""
+    if u.dtype not in _DT:
+        raise ValueError(f"unsupported I/O dtype {u.dtype}")
+    dev = u.device
+    b, dim, L = u.shape
+    N = A.shape[1]
+    io = u.dtype
+    _need(u, "u", (b, dim, L), io, dev)
+    _need(delta, "delta", (b, dim, L), io, dev)
+    _opt(z, "z", (b, dim, L), io, dev)
+    _need(B, "B", (b, N, L), io, dev)
+    _need(C, "C", (b, N, L), io, dev)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    _opt(D, "D", (dim,), torch.float32, dev)
+    _opt(delta_bias, "delta_bias", (dim,), torch.float32, dev)
+    _opt(h0, "h0", (b, dim, N), torch.float32, dev)
+    _need(y, "y", (b, dim, L), io, dev)
+    _opt(hL, "hL", (b, dim, N), torch.float32, dev)
+    p = capi.ScanParams()
+    p.batch, p.dim, p.dstate, p.seqlen = b, dim, N, L
+    p.io_dtype = _DT[io]
+    p.u, p.delta, p.z, p.B, p.C = _ptr(u), _ptr(delta), _ptr(z), _ptr(B), _ptr(C)
+    p.A, p.Dskip, p.delta_bias = _ptr(A), _ptr(D), _ptr(delta_bias)
+    p.delta_softplus = int(bool(delta_softplus))
+    p.zoh = int(bool(zoh))
+    p.h0, p.y, p.hL = _ptr(h0), _ptr(y), _ptr(hL)
+    p.chunk_len = int(chunk_len)
+    if workspace is not None:
+        p.workspace = workspace.data_ptr()
+        p.workspace_bytes = workspace.numel() * workspace.element_size()
+    return p
+
+
+def workspace_bytes(u, delta, A, B, C, chunk_len=0) -> int:
+    p = capi.ScanParams()
+    p.batch, p.dim, p.seqlen = u.shape
+    p.dstate = A.shape[1]
+    p.chunk_len = int(chunk_len)
+    n = capi.ssm_scan_workspace_size(p)
+    if n == 0:
+        raise ValueError("invalid scan sizes")
+    return n
+
+
+def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None, *,
+             delta_softplus=True, zoh=False, y=None, hL=None, return_last_state=True,
+             chunk_len=0, workspace=None, stream=None):
+    """Fused selective scan on the GPU.  Returns (y, hL) (hL None if not requested)."""
+    if y is None:
+        y = torch.empty_like(u)
+    if hL is None and return_last_state:
+        hL = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(u, delta, A, B, C, chunk_len), dtype=torch.uint8,
+                                device=u.device)
+    p = scan_params(u, delta, A, B, C, D, z, delta_bias, h0, y=y, hL=hL,
+                    delta_softplus=delta_softplus, zoh=zoh, chunk_len=chunk_len, workspace=workspace)
+    st = torch.cuda.current_stream(u.device).cuda_stream if stream is None else stream
+    capi.check(capi.ssm_scan_fwd(p, st), "ssm_scan_fwd")
+    return y, hL
+
+
+def step_params(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, *, y,
+                delta_softplus=True, zoh=False) -> capi.StepParams:
+    if u.dtype not in _DT:
+        raise ValueError(f"unsupported I/O dtype {u.dtype}")
+    dev = u.device
+    b, dim = u.shape
+    N = A.shape[1]
+    io = u.dtype
+    _need(state, "state", (b, dim, N), torch.float32, dev)
+    _need(u, "u", (b, dim), io, dev)
+    _need(delta, "delta", (b, dim), io, dev)
+    _opt(z, "z", (b, dim), io, dev)
+    _need(B, "B", (b, N), io, dev)
+    _need(C, "C", (b, N), io, dev)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    _opt(D, "D", (dim,), torch.float32, dev)
+    _opt(delta_bias, "delta_bias", (dim,), torch.float32, dev)
+    _need(y, "y", (b, dim), io, dev)
+    p = capi.StepParams()
+    p.batch, p.dim, p.dstate = b, dim, N
+    p.io_dtype = _DT[io]
+    p.state, p.u, p.delta, p.z = _ptr(state), _ptr(u), _ptr(delta), _ptr(z)
+    p.B, p.C, p.A, p.Dskip, p.delta_bias = _ptr(B), _ptr(C), _ptr(A), _ptr(D), _ptr(delta_bias)
+    p.delta_softplus = int(bool(delta_softplus))
+    p.zoh = int(bool(zoh))
+    p.y = _ptr(y)
+    return p
+
+
+def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, *,
+                 delta_softplus=True, zoh=False, y=None, stream=None):
+    """One decode token: updates ``state`` (b, D, N) fp32 in place, returns y (b, D)."""
+    if y is None:
+        y = torch.empty_like(u)
+    p = step_params(state, u, delta, A, B, C, D, z, delta_bias, y=y,
+                    delta_softplus=delta_softplus, zoh=zoh)
+    st = torch.cuda.current_stream(u.device).cuda_stream if stream is None else stream
+    capi.check(capi.ssm_state_update(p, st), "ssm_state_update")
+    return y
+
+
+def workspace_status(workspace, stream=None) -> int:
+    """Synchronise and return the device status recorded in a scan workspace."""
+    st = torch.cuda.current_stream(workspace.device).cuda_stream if stream is None else stream
+    return capi.ssm_workspace_status(workspace.data_ptr(), st)

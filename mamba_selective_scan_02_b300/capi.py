@@ -1,0 +1,119 @@
+"""ctypes view of libssmscan's C ABI (include/ssm_scan.h).
+
+Structs and prototypes mirror the header one to one.  The library is opened on
+first use from this package's ``lib/`` directory; if it is missing it is built
+in-tree with nvcc, and if that fails the call raises — there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT = range(5)
+SSM_F32, SSM_BF16 = 0, 1
+SSM_MAX_DSTATE = 16
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+class ScanParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("dstate", _i64), ("seqlen", _i64),
+        ("io_dtype", ctypes.c_int),
+        ("u", _vp), ("delta", _vp), ("z", _vp), ("B", _vp), ("C", _vp),
+        ("A", _vp), ("Dskip", _vp), ("delta_bias", _vp),
+        ("delta_softplus", ctypes.c_int), ("zoh", ctypes.c_int),
+        ("h0", _vp), ("y", _vp), ("hL", _vp),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("chunk_len", _i64),
+    ]
+
+
+class StepParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("dstate", _i64),
+        ("io_dtype", ctypes.c_int),
+        ("state", _vp), ("u", _vp), ("delta", _vp), ("z", _vp), ("B", _vp), ("C", _vp),
+        ("A", _vp), ("Dskip", _vp), ("delta_bias", _vp),
+        ("delta_softplus", ctypes.c_int), ("zoh", ctypes.c_int),
+        ("y", _vp),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded library (built in-tree first if absent or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if _build.stale(path):
+                _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"libssmscan is missing at {path} and could not be built")
+            L = ctypes.CDLL(path)
+            L.ssm_scan_workspace_size.restype = ctypes.c_size_t
+            L.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanParams)]
+            L.ssm_scan_fwd.restype = ctypes.c_int
+            L.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanParams), _vp]
+            L.ssm_state_update.restype = ctypes.c_int
+            L.ssm_state_update.argtypes = [ctypes.POINTER(StepParams), _vp]
+            L.ssm_workspace_status.restype = ctypes.c_int
+            L.ssm_workspace_status.argtypes = [_vp, _vp]
+            L.ssm_status_string.restype = ctypes.c_char_p
+            L.ssm_status_string.argtypes = [ctypes.c_int]
+            L.ssm_bench_mufu_ex2.restype = ctypes.c_int
+            L.ssm_bench_mufu_ex2.argtypes = [_vp, ctypes.c_int, ctypes.c_int, _vp]
+            L.ssm_version.restype = ctypes.c_char_p
+            L.ssm_version.argtypes = []
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().ssm_status_string(code).decode()
+
+
+class SSMError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+        self.code = code
+
+
+def check(code: int, where: str) -> None:
+    if code != SSM_OK:
+        raise SSMError(code, where)
+
+
+def ssm_scan_workspace_size(p: ScanParams) -> int:
+    return lib().ssm_scan_workspace_size(ctypes.byref(p))
+
+
+def ssm_scan_fwd(p: ScanParams, stream: int) -> int:
+    return lib().ssm_scan_fwd(ctypes.byref(p), stream)
+
+
+def ssm_state_update(p: StepParams, stream: int) -> int:
+    return lib().ssm_state_update(ctypes.byref(p), stream)
+
+
+def ssm_workspace_status(workspace: int, stream: int) -> int:
+    return lib().ssm_workspace_status(workspace, stream)
+
+
+def ssm_bench_mufu_ex2(sink: int, blocks: int, iters: int, stream: int) -> int:
+    return lib().ssm_bench_mufu_ex2(sink, blocks, iters, stream)

@@ -1,0 +1,187 @@
+// api.cu — the C ABI of libssmscan (declared in include/ssm_scan.h):
+// argument validation, workspace layout, launches on the caller's stream and
+// status reporting.  No entry point allocates memory.
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/ssm_scan.h"
+#include "ssm_internal.h"
+
+namespace {
+
+constexpr size_t kHeader = 256;  // status word + padding
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
+
+struct Layout {
+    int64_t chunk_len, nchunks;
+    size_t agg_off, carry_off, total;
+};
+
+bool scan_sizes_ok(const ssm_scan_params *p) {
+    if (!p) return false;
+    if (p->batch < 1 || p->dim < 1 || p->seqlen < 1 || p->dstate < 1) return false;
+    if (p->batch > 65535 || p->dim > (1 << 30) || p->seqlen > INT32_MAX) return false;
+    if (p->chunk_len < 0 || (p->chunk_len > 0 && p->chunk_len % 64 != 0)) return false;
+    return true;
+}
+
+Layout scan_layout(const ssm_scan_params *p) {
+    Layout l;
+    l.chunk_len = ssm::scan_chunk_len(p->batch, p->dim, p->dstate, p->seqlen, p->chunk_len);
+    l.nchunks = (p->seqlen + l.chunk_len - 1) / l.chunk_len;
+    const size_t bdn = (size_t)p->batch * p->dim * p->dstate;
+    l.agg_off = kHeader;
+    size_t agg_bytes = 0, carry_bytes = 0;
+    if (l.nchunks > 1) {
+        agg_bytes = align256(bdn * (size_t)(l.nchunks - 1) * sizeof(float2));
+        carry_bytes = align256(bdn * (size_t)l.nchunks * sizeof(float));
+    }
+    l.carry_off = l.agg_off + agg_bytes;
+    l.total = l.carry_off + carry_bytes;
+    return l;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_workspace_size(const ssm_scan_params *p) {
+    if (!scan_sizes_ok(p)) return 0;
+    return scan_layout(p).total;
+}
+
+ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream) {
+    if (!scan_sizes_ok(p)) return SSM_ERR_INVALID_ARG;
+    if (p->io_dtype != SSM_F32 && p->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (p->dstate > SSM_MAX_DSTATE) return SSM_ERR_UNSUPPORTED;
+    if (p->zoh != 0) return SSM_ERR_UNSUPPORTED;
+    if (p->delta_softplus != 0 && p->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (!p->u || !p->delta || !p->B || !p->C || !p->A || !p->y || !p->workspace) return SSM_ERR_INVALID_ARG;
+    const void *a16[] = {p->u, p->delta, p->z, p->B, p->C, p->y, p->h0, p->hL, p->workspace};
+    for (const void *q : a16)
+        if (q && !aligned16(q)) return SSM_ERR_INVALID_ARG;
+    const void *a4[] = {p->A, p->Dskip, p->delta_bias};
+    for (const void *q : a4)
+        if (q && !aligned4(q)) return SSM_ERR_INVALID_ARG;
+    const size_t es = p->io_dtype == SSM_BF16 ? 2 : 4;
+    const size_t seq = (size_t)p->batch * p->dim * p->seqlen * es;
+    const size_t bc = (size_t)p->batch * p->dstate * p->seqlen * es;
+    if (overlaps(p->y, seq, p->u, seq) || overlaps(p->y, seq, p->delta, seq) || overlaps(p->y, seq, p->z, seq) ||
+        overlaps(p->y, seq, p->B, bc) || overlaps(p->y, seq, p->C, bc))
+        return SSM_ERR_INVALID_ARG;
+    const Layout l = scan_layout(p);
+    if (p->workspace_bytes < l.total) return SSM_ERR_INVALID_ARG;
+    if (l.nchunks > 65535) return SSM_ERR_UNSUPPORTED;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(p->workspace);
+    if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+
+    ssm::ScanArgs a;
+    a.batch = (int)p->batch;
+    a.dim = (int)p->dim;
+    a.dstate = (int)p->dstate;
+    a.seqlen = (int)p->seqlen;
+    a.u = p->u;
+    a.delta = p->delta;
+    a.z = p->z;
+    a.B = p->B;
+    a.C = p->C;
+    a.A = p->A;
+    a.Dskip = p->Dskip;
+    a.bias = p->delta_bias;
+    a.delta_softplus = p->delta_softplus;
+    a.h0 = p->h0;
+    a.y = p->y;
+    a.hL = p->hL;
+    a.status = reinterpret_cast<int *>(ws);
+    a.agg = reinterpret_cast<float2 *>(ws + l.agg_off);
+    a.carry = reinterpret_cast<float *>(ws + l.carry_off);
+    a.chunk_len = (int)l.chunk_len;
+    a.nchunks = (int)l.nchunks;
+    return ssm::scan_launch(a, p->io_dtype == SSM_BF16, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_state_update(const ssm_step_params *p, ssm_stream_t stream) {
+    if (!p) return SSM_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->dim < 1 || p->dstate < 1) return SSM_ERR_INVALID_ARG;
+    if (p->batch * p->dim > (int64_t(1) << 31) / 4) return SSM_ERR_UNSUPPORTED;
+    if (p->io_dtype != SSM_F32 && p->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (p->dstate > SSM_MAX_DSTATE) return SSM_ERR_UNSUPPORTED;
+    if (p->zoh != 0) return SSM_ERR_UNSUPPORTED;
+    if (p->delta_softplus != 0 && p->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (!p->state || !p->u || !p->delta || !p->B || !p->C || !p->A || !p->y) return SSM_ERR_INVALID_ARG;
+    // The decode kernel reads every input with scalar loads, so element
+    // alignment is enough; the state is accessed 16 bytes at a time only when
+    // its base is 16-byte aligned and N is a multiple of 4.
+    const size_t es = p->io_dtype == SSM_BF16 ? 2 : 4;
+    const void *aio[] = {p->u, p->delta, p->z, p->B, p->C, p->y};
+    for (const void *q : aio)
+        if (q && (reinterpret_cast<uintptr_t>(q) % es) != 0) return SSM_ERR_INVALID_ARG;
+    const void *a4[] = {p->state, p->A, p->Dskip, p->delta_bias};
+    for (const void *q : a4)
+        if (q && !aligned4(q)) return SSM_ERR_INVALID_ARG;
+    const size_t nch = (size_t)p->batch * p->dim;
+    if (overlaps(p->y, nch * es, p->state, nch * p->dstate * 4) || overlaps(p->y, nch * es, p->u, nch * es) ||
+        overlaps(p->y, nch * es, p->delta, nch * es) || overlaps(p->y, nch * es, p->z, nch * es))
+        return SSM_ERR_INVALID_ARG;
+
+    ssm::StepArgs a;
+    a.batch = (int)p->batch;
+    a.dim = (int)p->dim;
+    a.dstate = (int)p->dstate;
+    a.state = p->state;
+    a.u = p->u;
+    a.delta = p->delta;
+    a.z = p->z;
+    a.B = p->B;
+    a.C = p->C;
+    a.A = p->A;
+    a.Dskip = p->Dskip;
+    a.bias = p->delta_bias;
+    a.delta_softplus = p->delta_softplus;
+    a.y = p->y;
+    return ssm::step_launch(a, p->io_dtype == SSM_BF16, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SSM_OK
+               : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_workspace_status(const void *workspace, ssm_stream_t stream) {
+    if (!workspace) return SSM_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SSM_ERR_CUDA;
+    int code = 0;
+    if (cudaMemcpy(&code, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SSM_ERR_CUDA;
+    return code == 0 ? SSM_OK : (code == SSM_ERR_TIMEOUT ? SSM_ERR_TIMEOUT : SSM_ERR_CUDA);
+}
+
+const char *ssm_status_string(ssm_status s) {
+    switch (s) {
+        case SSM_OK: return "ok";
+        case SSM_ERR_INVALID_ARG: return "invalid argument";
+        case SSM_ERR_UNSUPPORTED: return "unsupported by this build";
+        case SSM_ERR_CUDA: return "CUDA error";
+        case SSM_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+ssm_status ssm_bench_mufu_ex2(float *sink, int blocks, int iters, ssm_stream_t stream) {
+    if (!sink || blocks < 1 || iters < 1 || !aligned4(sink)) return SSM_ERR_INVALID_ARG;
+    return ssm::mufu_ex2_launch(sink, blocks, iters, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SSM_OK
+               : SSM_ERR_CUDA;
+}
+
+const char *ssm_version(void) { return "libssmscan sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,144 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects bad
+arguments before touching the GPU (these run without a GPU: every call below
+returns from host-side validation)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mamba_selective_scan_02_b300 import capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm_scan.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("ssm_scan_fwd", "ssm_state_update", "ssm_scan_workspace_size",
+                 "ssm_workspace_status", "ssm_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = capi.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ssm_scan.h but not exported"
+
+
+def test_library_is_in_tree():
+    assert os.path.dirname(capi.library_path()).startswith(ROOT)
+    assert capi.lib().ssm_version().decode().endswith("sm_103a")
+
+
+def test_status_strings():
+    for code in range(5):
+        assert capi.status_string(code)
+    assert capi.status_string(99) == "unknown status"
+
+
+FAKE = 0x10000000  # never dereferenced: every case below fails validation first
+
+
+def valid_scan(**over):
+    p = capi.ScanParams()
+    p.batch, p.dim, p.dstate, p.seqlen = 2, 64, 16, 256
+    p.io_dtype = capi.SSM_BF16
+    step = 1 << 20
+    p.u, p.delta, p.z, p.B, p.C = FAKE, FAKE + step, FAKE + 2 * step, FAKE + 3 * step, FAKE + 4 * step
+    p.A, p.Dskip, p.delta_bias = FAKE + 5 * step, FAKE + 6 * step, FAKE + 7 * step
+    p.delta_softplus = 1
+    p.y, p.hL, p.workspace = FAKE + 8 * step, FAKE + 9 * step, FAKE + 10 * step
+    p.workspace_bytes = 1 << 20
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(batch=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(seqlen=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(dstate=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(dstate=17), capi.SSM_ERR_UNSUPPORTED),
+    (dict(io_dtype=7), capi.SSM_ERR_INVALID_ARG),
+    (dict(u=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(A=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(workspace=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(u=FAKE + 2), capi.SSM_ERR_INVALID_ARG),           # not 16-byte aligned
+    (dict(hL=FAKE + 9 * (1 << 20) + 8), capi.SSM_ERR_INVALID_ARG),
+    (dict(A=FAKE + 5 * (1 << 20) + 1), capi.SSM_ERR_INVALID_ARG),
+    (dict(y=FAKE + 64), capi.SSM_ERR_INVALID_ARG),          # y overlaps u
+    (dict(workspace_bytes=16), capi.SSM_ERR_INVALID_ARG),   # smaller than the status word header
+    (dict(chunk_len=100), capi.SSM_ERR_INVALID_ARG),        # not a multiple of 64
+    (dict(chunk_len=-64), capi.SSM_ERR_INVALID_ARG),
+    (dict(delta_softplus=2), capi.SSM_ERR_INVALID_ARG),
+    (dict(zoh=1), capi.SSM_ERR_UNSUPPORTED),
+])
+def test_scan_rejects_before_launch(over, code):
+    assert capi.ssm_scan_fwd(valid_scan(**over), None) == code
+
+
+def test_scan_rejects_null_params():
+    assert capi.lib().ssm_scan_fwd(None, None) == capi.SSM_ERR_INVALID_ARG
+    assert capi.lib().ssm_scan_workspace_size(None) == 0
+
+
+def test_workspace_size():
+    p = valid_scan(chunk_len=0)
+    assert capi.ssm_scan_workspace_size(p) == 256          # one chunk: status word only
+    p = valid_scan(chunk_len=64)                             # 4 chunks of 64 tokens
+    bdn = 2 * 64 * 16
+    agg = -(-bdn * 3 * 8 // 256) * 256
+    carry = -(-bdn * 4 * 4 // 256) * 256
+    assert capi.ssm_scan_workspace_size(p) == 256 + agg + carry
+    # the small-model layer shape is split into chunks automatically
+    p = valid_scan(batch=2, dim=1536, seqlen=2048)
+    assert capi.ssm_scan_workspace_size(p) > 256
+    p = valid_scan(batch=4, dim=5120, seqlen=2048)
+    assert capi.ssm_scan_workspace_size(p) == 256
+    # too small a workspace is rejected
+    p = valid_scan(chunk_len=64, workspace_bytes=300)
+    assert capi.ssm_scan_fwd(p, None) == capi.SSM_ERR_INVALID_ARG
+
+
+def valid_step(**over):
+    p = capi.StepParams()
+    p.batch, p.dim, p.dstate = 4, 64, 16
+    p.io_dtype = capi.SSM_BF16
+    step = 1 << 20
+    p.state, p.u, p.delta, p.z = FAKE, FAKE + step, FAKE + 2 * step, FAKE + 3 * step
+    p.B, p.C, p.A = FAKE + 4 * step, FAKE + 5 * step, FAKE + 6 * step
+    p.delta_softplus = 1
+    p.y = FAKE + 7 * step
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(batch=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(dstate=17), capi.SSM_ERR_UNSUPPORTED),
+    (dict(state=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(state=FAKE + 2), capi.SSM_ERR_INVALID_ARG),      # fp32 state not 4-byte aligned
+    (dict(u=FAKE + (1 << 20) + 1), capi.SSM_ERR_INVALID_ARG),  # bf16 input at an odd address
+    (dict(y=FAKE + 1 * (1 << 20)), capi.SSM_ERR_INVALID_ARG),  # y is u
+    (dict(io_dtype=3), capi.SSM_ERR_INVALID_ARG),
+    (dict(zoh=1), capi.SSM_ERR_UNSUPPORTED),
+])
+def test_step_rejects_before_launch(over, code):
+    assert capi.ssm_state_update(valid_step(**over), None) == code
+
+
+def test_misc_rejections():
+    lib = capi.lib()
+    assert lib.ssm_state_update(None, None) == capi.SSM_ERR_INVALID_ARG
+    assert lib.ssm_workspace_status(None, None) == capi.SSM_ERR_INVALID_ARG
+    assert lib.ssm_bench_mufu_ex2(None, 1, 1, None) == capi.SSM_ERR_INVALID_ARG
+    assert lib.ssm_bench_mufu_ex2(ctypes.c_void_p(FAKE), 0, 1, None) == capi.SSM_ERR_INVALID_ARG
