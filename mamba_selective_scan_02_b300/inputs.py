@@ -66,12 +66,12 @@ def s4d_real_A(dim: int, dstate: int, device="cpu") -> torch.Tensor:
     return -torch.arange(1, dstate + 1, dtype=torch.float32, device=device).repeat(dim, 1).contiguous()
 
 
-def _bias(w: Workload, g: torch.Generator, device) -> torch.Tensor:
+def _bias(w: Workload, dim: int, g: torch.Generator, device) -> torch.Tensor:
     if w.bias == "const-1":
-        return torch.full((w.dim,), -1.0, dtype=torch.float32, device=device)
+        return torch.full((dim,), -1.0, dtype=torch.float32, device=device)
     # bias_d = log(expm1(U_d)) with U_d ~ Uniform[1e-3, 1e-1]: the inverse of the
     # softplus, so that softplus(bias_d) = U_d is the channel's resting step size.
-    U = torch.empty(w.dim, dtype=torch.float64, device=device)
+    U = torch.empty(dim, dtype=torch.float64, device=device)
     U.uniform_(1e-3, 1e-1, generator=g)
     return torch.log(torch.expm1(U)).float()
 
@@ -115,7 +115,7 @@ def make_inputs(w: Workload | str, device="cpu", batch: int | None = None,
     B = normal(bc_shape)
     C = normal(bc_shape)
     Dskip = torch.randn(D, generator=g, dtype=torch.float32, device=device)
-    bias = _bias(w, g, device)
+    bias = _bias(w, D, g, device)
     h0 = None
     if w.h0_std > 0:
         h0 = torch.randn((b, D, N), generator=g, dtype=torch.float32, device=device) * w.h0_std
