@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--settle-s", type=float, default=0.5,
+                    help="seconds of untimed load before the timed region (clock settling)")
     return ap.parse_args()
 
 
@@ -55,28 +57,38 @@ def measured_peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """Polls SM clock and clock-event reasons through NVML (read-only) in a thread."""
+    """Samples SM clock and clock-event reasons during the timed region (read-only).
+
+    Uses NVML through pynvml when it is importable, else a ``nvidia-smi
+    --query-gpu ... -lms`` child process; both only read the GPU's state."""
 
     REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
                0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ("clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+                  "clocks_event_reasons.hw_thermal_slowdown",
+                  "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, torch_index: int, period_s: float = 0.02):
-        self.samples, self.period, self.ok = [], period_s, False
+    def __init__(self, torch_index: int, period_s: float = 0.05):
+        self.samples, self.period, self.ok, self.mode = [], period_s, False, None
+        self.max_mhz = None
         self._stop = threading.Event()
+        import torch
+        uuid = str(torch.cuda.get_device_properties(torch_index).uuid)
+        self.uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
         try:
             import pynvml
-            import torch
             pynvml.nvmlInit()
-            uuid = str(torch.cuda.get_device_properties(torch_index).uuid)
-            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid)
             self.nv = pynvml
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # pragma: no cover - reported in the JSON
+            self.ok, self.mode = True, "nvml"
+        except Exception as e:
             self.err = repr(e)
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.ok, self.mode = True, "nvidia-smi"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
@@ -88,15 +100,38 @@ class ClockSampler:
             time.sleep(self.period)
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self.t = threading.Thread(target=self._run_nvml, daemon=True)
             self.t.start()
+        elif self.mode == "nvidia-smi":
+            import subprocess
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid, "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", str(int(self.period * 1000))],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         return self
 
     def __exit__(self, *a):
         self._stop.set()
-        if self.ok:
+        if self.mode == "nvml":
             self.t.join()
+        elif self.mode == "nvidia-smi":
+            self.proc.terminate()
+            out, _ = self.proc.communicate()
+            bits = {2: 0x8, 3: 0x40, 4: 0x20, 5: 0x4}
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) != len(self.SMI_FIELDS):
+                    continue
+                try:
+                    mhz, self.max_mhz = float(f[0]), float(f[1])
+                except ValueError:
+                    continue
+                mask = 0
+                for i, bit in bits.items():
+                    if f[i].lower() == "active":
+                        mask |= bit
+                self.samples.append((mhz, mask))
 
     def summary(self):
         if not self.ok or not self.samples:
@@ -107,13 +142,15 @@ class ClockSampler:
             mask |= r
         return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
                 "reasons": sorted(v for k, v in self.REASONS.items() if mask & k),
-                "samples": len(self.samples)}
+                "samples": len(self.samples), "source": self.mode}
 
 
 # ------------------------------------------------------------------ CPU oracle
 def oracle_rate(w, seconds: float, cores: int, seed_offset: int = 0):
-    """Gelem/s of the fp64 oracle on a bounded sample of ``w``'s channels: the
-    unchanged sequential oracle, its independent channels split over host threads."""
+    """Gelem/s of the fp64 oracle on a bounded sample of ``w``: the unchanged
+    sequential oracle, its independent (b, d) channels split over host threads.
+    The sample is the first ``dim`` channels of one sequence (all L tokens),
+    repeated until about ``seconds`` of CPU work has been timed."""
     from mamba_selective_scan_02_b300.inputs import make_inputs
     from oracle import oracle as orc
 
@@ -125,12 +162,16 @@ def oracle_rate(w, seconds: float, cores: int, seed_offset: int = 0):
     rounds = max(1, int(seconds / per_round))
     dim = min(w.dim, cores * rounds)
     inp = make_inputs(w, batch=1, dim=dim, seed=w.seed + 2000 + seed_offset)
-    t0 = time.perf_counter()
-    orc.scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], Dskip=inp["Dskip"], z=inp["z"],
-             bias=inp["bias"], threads=cores)
-    dt = time.perf_counter() - t0
-    elems = dim * w.seqlen
-    return elems / dt / 1e9, dt, f"{dim} channels x {w.seqlen} tokens (N={w.dstate}) of {w.name}"
+    reps, dt = 0, 0.0
+    while reps == 0 or dt < 0.8 * seconds:
+        t0 = time.perf_counter()
+        orc.scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], Dskip=inp["Dskip"], z=inp["z"],
+                 bias=inp["bias"], threads=cores)
+        dt += time.perf_counter() - t0
+        reps += 1
+    elems = reps * dim * w.seqlen
+    return elems / dt / 1e9, dt, (f"{reps} x ({dim} channels x {w.seqlen} tokens, N={w.dstate}) "
+                                  f"of {w.name}")
 
 
 def run_reference(args):
@@ -233,7 +274,7 @@ def run_ours(args):
     clocks = ClockSampler(local)
     with clocks:
         # keep warming until clocks settle (>= 0.5 s of load), then time exactly K steps
-        t_end = time.perf_counter() + 0.5
+        t_end = time.perf_counter() + args.settle_s
         while time.perf_counter() < t_end:
             for _ in range(50):
                 capi.ssm_scan_fwd(p, sh)
