@@ -120,6 +120,34 @@ typedef struct {
 /* One decode token for every (b, d): the recurrence with L = 1 on `state`. */
 ssm_status ssm_state_update(const ssm_step_params *p, ssm_stream_t stream);
 
+/* Size of the scratch array that ssm_scan_fwd_noalloc keeps inside the
+ * library (16 MiB, held on every GPU that loads the library until exit). */
+#define SSM_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* ssm_scan_fwd for callers that cannot allocate device memory at all (a
+ * plugin whose host framework owns every allocation and offers it no
+ * allocator, or a loop that must not call cudaMalloc because it can
+ * synchronise the device).  The pages have no counterpart; it is a service of
+ * this library.
+ *
+ * It computes exactly what ssm_scan_fwd computes, but the chunk scratch lives
+ * in a fixed device array of SSM_NOALLOC_SCRATCH_BYTES inside the library, so
+ * p->workspace and p->workspace_bytes are ignored.  It allocates nothing and
+ * frees nothing.
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - Sizes whose scratch need (ssm_scan_workspace_size) exceeds
+ *     SSM_NOALLOC_SCRATCH_BYTES are rejected with SSM_ERR_UNSUPPORTED before
+ *     anything is launched; other argument errors are those of ssm_scan_fwd.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents.  Calls whose work overlaps on the GPU (different
+ *     streams, not ordered by events) race on it: serialise them.
+ *   - A device-side timeout is recorded in the shared array, where
+ *     ssm_workspace_status cannot reach it; callers that need that report use
+ *     ssm_scan_fwd with their own workspace. */
+ssm_status ssm_scan_fwd_noalloc(const ssm_scan_params *p, ssm_stream_t stream);
+
 /* Synchronises `stream`, then returns SSM_OK or the error a kernel recorded in
  * this workspace (SSM_ERR_TIMEOUT), or SSM_ERR_CUDA if the copy fails. */
 ssm_status ssm_workspace_status(const void *workspace, ssm_stream_t stream);

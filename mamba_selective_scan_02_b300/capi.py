@@ -16,6 +16,7 @@ from . import build as _build
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT = range(5)
 SSM_F32, SSM_BF16 = 0, 1
 SSM_MAX_DSTATE = 16
+SSM_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -70,6 +71,8 @@ def lib():
             L.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanParams)]
             L.ssm_scan_fwd.restype = ctypes.c_int
             L.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanParams), _vp]
+            L.ssm_scan_fwd_noalloc.restype = ctypes.c_int
+            L.ssm_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ScanParams), _vp]
             L.ssm_state_update.restype = ctypes.c_int
             L.ssm_state_update.argtypes = [ctypes.POINTER(StepParams), _vp]
             L.ssm_workspace_status.restype = ctypes.c_int
@@ -105,6 +108,10 @@ def ssm_scan_workspace_size(p: ScanParams) -> int:
 
 def ssm_scan_fwd(p: ScanParams, stream: int) -> int:
     return lib().ssm_scan_fwd(ctypes.byref(p), stream)
+
+
+def ssm_scan_fwd_noalloc(p: ScanParams, stream: int) -> int:
+    return lib().ssm_scan_fwd_noalloc(ctypes.byref(p), stream)
 
 
 def ssm_state_update(p: StepParams, stream: int) -> int:
