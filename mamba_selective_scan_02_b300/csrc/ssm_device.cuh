@@ -52,6 +52,31 @@ __device__ __forceinline__ float softplus(float x) {
     return fmaxf(x, 0.0f) + (w < 0.0625f ? series : viaLog);
 }
 
+// log1p(w) for w in [0, 1] on the FMA pipe only: w·q(w), q of degree 7 fitted
+// to log1p(w)/w towards minimax relative error (csrc/fit_log1p.py prints the
+// coefficients); relative error 3.7e-7 in fp32.
+__device__ __forceinline__ float log1p_unit(float w) {
+    float q = fmaf(w, -0.008539210073649883f, 0.04408963769674301f);
+    q = fmaf(w, q, -0.10768172144889832f);
+    q = fmaf(w, q, 0.17745241522789001f);
+    q = fmaf(w, q, -0.24495463073253632f);
+    q = fmaf(w, q, 0.33275479078292847f);
+    q = fmaf(w, q, -0.4999740421772003f);
+    q = fmaf(w, q, 0.9999998211860657f);
+    return w * q;
+}
+// Branch-free softplus, one MUFU op: max(x, 0) + log1p(e^{-|x|}).
+__device__ __forceinline__ float softplus_poly(float x) {
+    return fmaxf(x, 0.0f) + log1p_unit(ex2(-fabsf(x) * kLog2e));
+}
+// Two MUFU ops, four FMA-pipe ops: log1p(w) = ln2·lg2(1 + w).  The rounding of
+// 1 + w and lg2.approx leave an absolute error near 2e-7 in Δ, far below the
+// bf16 rounding of the inputs it is used with.
+__device__ __forceinline__ float softplus_mufu(float x) {
+    const float w = ex2(-fabsf(x) * kLog2e);
+    return fmaf(lg2(1.0f + w), kLn2, fmaxf(x, 0.0f));
+}
+
 // silu(z) = z·σ(z).  Accurate form (fp32 I/O): z / (1 + 2^{-z·log2e}).
 __device__ __forceinline__ float silu_accurate(float z) {
     return z * rcp_approx(1.0f + ex2(-z * kLog2e));
@@ -69,11 +94,34 @@ template <> struct IO<float> {
     __device__ __forceinline__ static float to_f(float v) { return v; }
     __device__ __forceinline__ static float from_f(float v) { return v; }
     static constexpr bool kFastGate = false;
+    // 8 consecutive values from shared memory (16-byte aligned) to fp32.
+    __device__ __forceinline__ static void load8(const float *p, float *o) {
+        const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    }
+    __device__ __forceinline__ static float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+    __device__ __forceinline__ static void store2(float *p, float2 v) { *reinterpret_cast<float2 *>(p) = v; }
+    __device__ __forceinline__ static float softplus(float x) { return softplus_poly(x); }
 };
 template <> struct IO<__nv_bfloat16> {
     __device__ __forceinline__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
     __device__ __forceinline__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
     static constexpr bool kFastGate = true;
+    __device__ __forceinline__ static float lo(uint32_t w) { return __uint_as_float(w << 16); }
+    __device__ __forceinline__ static float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+    __device__ __forceinline__ static void load8(const __nv_bfloat16 *p, float *o) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p);
+        o[0] = lo(v.x); o[1] = hi(v.x); o[2] = lo(v.y); o[3] = hi(v.y);
+        o[4] = lo(v.z); o[5] = hi(v.z); o[6] = lo(v.w); o[7] = hi(v.w);
+    }
+    __device__ __forceinline__ static float4 load4(const __nv_bfloat16 *p) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        return make_float4(lo(v.x), hi(v.x), lo(v.y), hi(v.y));
+    }
+    __device__ __forceinline__ static void store2(__nv_bfloat16 *p, float2 v) {
+        *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(v.x, v.y);
+    }
+    __device__ __forceinline__ static float softplus(float x) { return softplus_mufu(x); }
 };
 
 template <typename T>
