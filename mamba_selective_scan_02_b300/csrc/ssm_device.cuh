@@ -128,6 +128,15 @@ template <typename T>
 __device__ __forceinline__ float gate_of(float z) {
     return IO<T>::kFastGate ? silu_fast(z) : silu_accurate(z);
 }
+// silu of two values; the fast form runs its multiply-adds packed.
+template <typename T>
+__device__ __forceinline__ float2 gate2(float2 z) {
+    if (IO<T>::kFastGate) {
+        const float2 hz = __fmul2_rn(z, make_float2(0.5f, 0.5f));
+        return __ffma2_rn(hz, make_float2(tanh_approx(hz.x), tanh_approx(hz.y)), hz);
+    }
+    return make_float2(silu_accurate(z.x), silu_accurate(z.y));
+}
 
 // ---------------------------------------------------------------- mbarrier / TMA
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -183,6 +192,10 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until at most one committed bulk group is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
