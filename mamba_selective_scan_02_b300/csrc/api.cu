@@ -16,8 +16,8 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
 
 struct Layout {
-    int64_t chunk_len, nchunks;
-    size_t agg_off, carry_off, total;
+    ssm::ScanPlan plan;
+    size_t flags_off, agg_off, carry_off, zero_bytes, total;
 };
 
 bool scan_sizes_ok(const ssm_scan_params *p) {
@@ -28,19 +28,28 @@ bool scan_sizes_ok(const ssm_scan_params *p) {
     return true;
 }
 
+// Workspace: a 256-byte header (status word, two work counters), then
+//   chained:  one int flag per channel group, and one b × D × N fp32 state;
+//   two-pass: per-chunk aggregates [b][D][K-1][N] (float2) and carried states
+//             [b][D][K][N] (fp32).
+// The header and the flags are cleared before every launch.
 Layout scan_layout(const ssm_scan_params *p) {
     Layout l;
-    l.chunk_len = ssm::scan_chunk_len(p->batch, p->dim, p->dstate, p->seqlen, p->chunk_len);
-    l.nchunks = (p->seqlen + l.chunk_len - 1) / l.chunk_len;
+    l.plan = ssm::scan_plan(p->batch, p->dim, p->dstate, p->seqlen, p->chunk_len);
     const size_t bdn = (size_t)p->batch * p->dim * p->dstate;
-    l.agg_off = kHeader;
-    size_t agg_bytes = 0, carry_bytes = 0;
-    if (l.nchunks > 1) {
-        agg_bytes = align256(bdn * (size_t)(l.nchunks - 1) * sizeof(float2));
-        carry_bytes = align256(bdn * (size_t)l.nchunks * sizeof(float));
+    l.flags_off = l.agg_off = l.carry_off = kHeader;
+    l.zero_bytes = kHeader;
+    l.total = kHeader;
+    if (l.plan.chained) {
+        const size_t flag_bytes = align256((size_t)l.plan.groups * sizeof(int));
+        l.carry_off = kHeader + flag_bytes;
+        l.zero_bytes = kHeader + flag_bytes;
+        l.total = l.carry_off + align256(bdn * sizeof(float));
+    } else if (l.plan.nchunks > 1) {
+        const size_t agg_bytes = align256(bdn * (size_t)(l.plan.nchunks - 1) * sizeof(float2));
+        l.carry_off = kHeader + agg_bytes;
+        l.total = l.carry_off + align256(bdn * (size_t)l.plan.nchunks * sizeof(float));
     }
-    l.carry_off = l.agg_off + agg_bytes;
-    l.total = l.carry_off + carry_bytes;
     return l;
 }
 
@@ -80,11 +89,11 @@ ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream) {
         return SSM_ERR_INVALID_ARG;
     const Layout l = scan_layout(p);
     if (p->workspace_bytes < l.total) return SSM_ERR_INVALID_ARG;
-    if (l.nchunks > 65535) return SSM_ERR_UNSUPPORTED;
+    if (l.plan.groups * l.plan.nchunks > INT32_MAX / 2) return SSM_ERR_UNSUPPORTED;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     unsigned char *ws = static_cast<unsigned char *>(p->workspace);
-    if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, l.zero_bytes, st) != cudaSuccess) return SSM_ERR_CUDA;
 
     ssm::ScanArgs a;
     a.batch = (int)p->batch;
@@ -104,10 +113,14 @@ ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream) {
     a.y = p->y;
     a.hL = p->hL;
     a.status = reinterpret_cast<int *>(ws);
+    a.tickets = reinterpret_cast<int *>(ws) + 1;
+    a.flags = reinterpret_cast<int *>(ws + l.flags_off);
     a.agg = reinterpret_cast<float2 *>(ws + l.agg_off);
     a.carry = reinterpret_cast<float *>(ws + l.carry_off);
-    a.chunk_len = (int)l.chunk_len;
-    a.nchunks = (int)l.nchunks;
+    a.chunk_len = (int)l.plan.chunk_len;
+    a.nchunks = (int)l.plan.nchunks;
+    a.groups = (int)l.plan.groups;
+    a.chained = l.plan.chained ? 1 : 0;
     return ssm::scan_launch(a, p->io_dtype == SSM_BF16, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

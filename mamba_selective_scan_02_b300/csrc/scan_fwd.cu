@@ -7,142 +7,157 @@
 //   y = (C·h + D·u)·silu(z),
 // writing only y (b × D × L) and the final state — never Ā, B̄ or any h_t.
 //
-// Design (B300-first, not the pages' kernel).  On this part one state update
-// costs one MUFU exponential and four FP32 operations (Δ·A, B·Δu, Ā·h + B̄u,
-// C·h); the SM retires 32 exponentials but only 128 FP32 lanes per clock, and
-// issues one instruction per scheduler per clock, so the kernel is built to
-// spend as few instructions per state update as possible:
-//   * Channels are the parallel axis.  A thread owns SPT consecutive states of
-//     one channel and walks the time axis sequentially with them in registers;
-//     NG = N/SPT adjacent lanes share a channel.  State arithmetic is packed
-//     f32x2 (two states per instruction); Ā is ex2.approx on Δ·A·log2e.
-//   * Per tile of TT tokens, one elected thread moves u, Δraw, z (CH channels ×
-//     TT tokens) and B, C (N × TT, shared by every channel of the CTA) into
-//     shared memory with 3-D TMA copies on an mbarrier; the y tile leaves with
-//     a TMA store.  The next tile's copies overlap the current tile's scan.
-//   * Three phases per tile.  Pre-pass: the per-token nonlinearities (softplus,
-//     Δ·u, silu(z), D·u·gate) once per (channel, token), and B, C widened to
-//     fp32 in token-major rows so a thread reads its states with one 16-byte
-//     load.  Scan: only loads of those fp32 rows, packed FMAs and ex2; each lane
-//     leaves its partial C·h per token in shared memory.  Epilogue: the NG
-//     partials of a token are added, gated, rounded and staged for the store.
-//   * Long sequences are cut into chunks that run concurrently.  The
-//     composition of affine steps is associative (first-principles page,
-//     "The hardware-aware scan"): an aggregate pass computes each chunk's pair
-//     (Π Ā, h_end from zero), a carry pass chains the pairs from h0, and the
-//     main pass rescans every chunk from its carried state.
+// Design (B300-first, not the pages' kernel).  One state update costs one
+// MUFU exponential and four FP32 operations (Δ·A, B·Δu, Ā·h + B̄u, C·h).  On
+// this part the FP32 pipe and the MUFU are both busy at the same rate, and a
+// scheduler needs at least two resident warps to keep them fed, so:
+//   * A warp owns a group of CPW channels; NG = 1 or 2 lanes share a channel
+//     and each lane keeps SPT of its states in registers (packed f32x2 math,
+//     Ā = ex2.approx of Δ·A·log2e) while walking the time axis in order.
+//     With two lanes per channel the per-token partial sums C·h are combined
+//     with a transposed shuffle over four tokens.
+//   * Each lane forms softplus(Δraw + bias), Δ·u, silu(z) and D·u·silu(z) for
+//     its channel straight from the staged bf16/fp32 tile in registers; no
+//     per-token intermediate goes through shared memory.
+//   * Warps are persistent and take work items — (channel group, chunk of the
+//     sequence) — from a counter.  Chained mode hands items out chunk-major,
+//     and chunk k of a group starts from the state chunk k-1 published
+//     (waiting on a flag, with a bounded spin): every warp stays busy until
+//     the end whatever the channel count, with no extra pass.  When there are
+//     too few groups to fill the GPU, two-pass mode cuts the sequence into
+//     chunks that run at once: an aggregate pass computes each chunk's pair
+//     (Π Ā, h_end from zero), a carry pass chains the pairs from h0 (the
+//     affine composition of first-principles page, "The hardware-aware scan"),
+//     and the main pass rescans every chunk from its carried state.
+//   * Per tile of TT tokens one lane moves u, Δraw, z (as 8-token × CPW-channel
+//     boxes) and B, C (N × TT, shared by every channel) into shared memory with
+//     TMA on an mbarrier, two stages deep; the next tile — of the same item or
+//     of the next item — loads while this one is scanned.  y leaves with TMA
+//     stores from a double-buffered tile.
 #include <algorithm>
 #include <cstring>
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
-#ifndef SSM_SCAN_TT
-#define SSM_SCAN_TT 32
-#endif
-
 namespace ssm {
 
-constexpr int kTT = SSM_SCAN_TT;       // tokens per tile (a multiple of 8; chunks are multiples of 64)
-constexpr int kCH = 32;                // channels per CTA: one warp, one lane per channel
+constexpr int kTT = 32;                // tokens per tile (chunks are multiples of 64)
+constexpr int kWarpsPerSM = 8;         // resident warps targeted per SM (2 per scheduler)
+constexpr int kSMs = 148;              // B300
 constexpr int kWaitLimit = 1 << 22;    // mbarrier polls before giving up
+constexpr int kFlagLimit = 1 << 24;    // polls of a predecessor's flag before giving up
+constexpr int kDefaultChunk = 256;     // tokens per work item in chained mode
 
 __host__ __device__ constexpr int al128(int x) { return (x + 127) / 128 * 128; }
 
-// Shared-memory layout of one CTA (byte offsets; TMA destinations 128-B aligned).
-// u, Δraw, z and y tiles are stored as [TT/8][32 channels][8 tokens] so that a
-// lane's 8 tokens are one contiguous 16-byte (bf16) or 32-byte (fp32) run and a
-// warp's loads cover consecutive banks; each such block is one TMA box.
-template <typename T, int SPT, int TT> struct WTile {
-    static_assert(SPT % 4 == 0 && TT % 8 == 0, "tile shape");
+// Shared-memory layout of one warp's CTA (byte offsets; TMA destinations 128-B
+// aligned).  u, Δraw, z and y tiles are stored as [TT/8][CPW channels][8 tokens]:
+// a channel's 8 tokens are one contiguous 16-byte (bf16) or 32-byte (fp32) run
+// and each [CPW][8] block is one TMA box.
+template <typename T, int SPT, int NG> struct WTile {
+    static_assert(SPT % 4 == 0 && (NG == 1 || NG == 2), "tile shape");
+    static constexpr int CPW = 32 / NG;           // channels per warp
+    static constexpr int NP = SPT * NG;           // states covered (>= N)
     static constexpr int ES = (int)sizeof(T);
-    static constexpr int NB8 = TT / 8;            // 8-token blocks per tile
-    static constexpr int BLK = kCH * 8 * ES;      // one 8-token block of one input
+    static constexpr int NB8 = kTT / 8;           // 8-token blocks per tile
+    static constexpr int BLK = CPW * 8 * ES;      // one 8-token block of one input
     static constexpr int SEQ = NB8 * BLK;         // one input tile
-    static constexpr int BC = SPT * TT * ES;      // one B or C tile (N <= SPT rows)
-    static constexpr int BCP = SPT + 4;           // fp32 B/C row pitch in floats (16-B rows)
+    static constexpr int BC = NP * kTT * ES;      // one B or C tile (N <= NP rows)
+    static constexpr int BCP = NP + 4;            // fp32 B/C row pitch in floats (16-B rows)
     static constexpr int BUF = 3 * al128(SEQ) + 2 * al128(BC);  // one stage: u, Δ, z, B, C
     static constexpr int off_u = 0, off_d = al128(SEQ), off_z = 2 * al128(SEQ);
     static constexpr int off_B = 3 * al128(SEQ), off_C = off_B + al128(BC);
+    static constexpr int OUT = al128(SEQ);                       // one y tile
     static constexpr int off_out = 2 * BUF;                      // two y tiles
-    static constexpr int off_Bf = off_out + 2 * al128(SEQ);
-    static constexpr int off_Cf = off_Bf + al128(TT * BCP * 4);
-    static constexpr int off_bar = off_Cf + al128(TT * BCP * 4);
+    static constexpr int off_Bf = off_out + 2 * OUT;
+    static constexpr int off_Cf = off_Bf + al128(kTT * BCP * 4);
+    static constexpr int off_bar = off_Cf + al128(kTT * BCP * 4);
     static constexpr int bytes = off_bar + 16;
-    static constexpr int OUT = al128(SEQ);        // one y tile
 };
 
 struct Maps {
     CUtensorMap u, d, z, B, C, y;
 };
 
-template <typename T> struct Pack8;
-template <> struct Pack8<float> {
-    __device__ __forceinline__ static void store(float *p, const float *v) {
+template <typename T> struct Pack;
+template <> struct Pack<float> {
+    __device__ __forceinline__ static void store8(float *p, const float *v) {
         reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
         reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
+    __device__ __forceinline__ static void store2(float *p, float2 v) { *reinterpret_cast<float2 *>(p) = v; }
 };
-template <> struct Pack8<__nv_bfloat16> {
+template <> struct Pack<__nv_bfloat16> {
     __device__ __forceinline__ static uint32_t pk(float a, float b) {
         const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
         return *reinterpret_cast<const uint32_t *>(&v);
     }
-    __device__ __forceinline__ static void store(__nv_bfloat16 *p, const float *v) {
+    __device__ __forceinline__ static void store8(__nv_bfloat16 *p, const float *v) {
         *reinterpret_cast<uint4 *>(p) = make_uint4(pk(v[0], v[1]), pk(v[2], v[3]), pk(v[4], v[5]), pk(v[6], v[7]));
+    }
+    __device__ __forceinline__ static void store2(__nv_bfloat16 *p, float2 v) {
+        *reinterpret_cast<uint32_t *>(p) = pk(v.x, v.y);
     }
 };
 
-// MODE 0: full scan writing y (and hL for the last chunk).
-// MODE 1: chunk aggregate (Π Ā, h_end from zero) for chunks 0..K-2.
-// One warp per CTA; lane c owns channel d0 + c and all SPT (>= N) of its states.
-template <typename T, int SPT, int TT, bool HAS_Z, bool TMA, int MODE>
-__global__ void __launch_bounds__(kCH, 1)
+__device__ __forceinline__ int ld_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(int *p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// One work item: a group of CPW channels of one sequence, one chunk of tokens.
+struct Item {
+    int grp, k, b, d0, t_begin, t_end, ntiles;
+};
+
+// MODE 0: scan writing y (and hL after the last chunk).
+// MODE 1: chunk aggregate (Π Ā, h_end from zero) for chunks 0..K-2 (two-pass).
+template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, int MODE>
+__global__ void __launch_bounds__(32, 1)
 scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
-    using S = WTile<T, SPT, TT>;
-    constexpr int NQ = SPT / 2;      // float2 state pairs per lane
-    constexpr int NB8 = S::NB8;
+    using S = WTile<T, SPT, NG>;
+    constexpr int CPW = S::CPW, NB8 = S::NB8, NQ = SPT / 2;
+    constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(128) unsigned char smem[];
     float *Bf = reinterpret_cast<float *>(smem + S::off_Bf);
     float *Cf = reinterpret_cast<float *>(smem + S::off_Cf);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::off_bar);
 
     const int lane = threadIdx.x;
-    const int d0 = blockIdx.x * kCH;
-    const int b = blockIdx.y;
-    const int k = blockIdx.z;        // chunk
+    const int c = lane / NG;          // channel within the group
+    const int g = lane % NG;          // which SPT states of the channel
     const int D = a.dim, N = a.dstate, L = a.seqlen;
-    const int d = d0 + lane;
-    const bool live = d < D;
-    const int t_begin = k * a.chunk_len;
-    const int t_end = min(L, t_begin + a.chunk_len);
-    const int ntiles = (t_end - t_begin + TT - 1) / TT;
+    const int gpb = (D + CPW - 1) / CPW;  // groups per sequence
+    const int K = a.nchunks;
+    const int kitems = MODE == 0 ? K : K - 1;
+    const int items = a.groups * kitems;
+    int *ticket = a.tickets + (MODE == 0 ? 0 : 1);
+    const bool chained = MODE == 0 && a.chained;
 
-    // ---- per-lane constants: A·log2e for the channel's states, initial state
-    float2 A2[NQ], h[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        float av[2] = {0.f, 0.f}, hv[2] = {0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int n = 2 * q + j;
-            if (live && n < N) {
-                av[j] = a.A[(size_t)d * N + n] * kLog2e;
-                if (MODE == 0) {
-                    // With several chunks h0 is read only by the carry pass, so
-                    // hL may share h0's buffer.
-                    if (a.nchunks > 1)
-                        hv[j] = a.carry[(((size_t)b * D + d) * a.nchunks + k) * N + n];
-                    else if (a.h0)
-                        hv[j] = a.h0[((size_t)b * D + d) * N + n];
-                }
-            }
-        }
-        A2[q] = make_float2(av[0], av[1]);
-        h[q] = make_float2(hv[0], hv[1]);
-    }
-    const float bias = (live && a.bias) ? a.bias[d] : 0.f;
-    const float skip = (live && a.Dskip) ? a.Dskip[d] : 0.f;
+    auto item_of = [&](int t) {
+        Item it;
+        // Chained items go out chunk-major, so a chunk's predecessor was handed
+        // out a full round of groups earlier.
+        it.k = t / a.groups;
+        it.grp = t % a.groups;
+        it.b = it.grp / gpb;
+        it.d0 = (it.grp % gpb) * CPW;
+        it.t_begin = it.k * a.chunk_len;
+        it.t_end = min(L, it.t_begin + a.chunk_len);
+        it.ntiles = (it.t_end - it.t_begin + kTT - 1) / kTT;
+        return it;
+    };
+    auto grab = [&]() {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(ticket, 1);
+        return __shfl_sync(FULL, t, 0);
+    };
+
     if (TMA && lane == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
@@ -150,241 +165,355 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     }
     __syncwarp();
 
-    const uint32_t bc_bytes = (uint32_t)N * TT * sizeof(T);
-    auto stage = [&](int buf) { return smem + buf * S::BUF; };
-    auto issue_loads = [&](int tile, int buf) {
-        const int t0 = t_begin + tile * TT;
-        unsigned char *st = stage(buf);
+    const uint32_t bc_bytes = (uint32_t)N * kTT * sizeof(T);
+    auto stage = [&](int s) { return smem + s * S::BUF; };
+    auto issue_loads = [&](const Item &it, int tile, int s) {
+        const int t0 = it.t_begin + tile * kTT;
+        unsigned char *st = stage(s);
         const uint32_t bytes = (MODE == 0 ? (HAS_Z ? 3u : 2u) : 2u) * S::SEQ + (MODE == 0 ? 2u : 1u) * bc_bytes;
-        mbar_arrive_expect_tx(&bar[buf], bytes);
+        mbar_arrive_expect_tx(&bar[s], bytes);
 #pragma unroll
         for (int j = 0; j < NB8; ++j) {
-            tma_load_3d(st + S::off_u + j * S::BLK, &maps.u, &bar[buf], t0 + 8 * j, d0, b);
-            tma_load_3d(st + S::off_d + j * S::BLK, &maps.d, &bar[buf], t0 + 8 * j, d0, b);
-            if (MODE == 0 && HAS_Z) tma_load_3d(st + S::off_z + j * S::BLK, &maps.z, &bar[buf], t0 + 8 * j, d0, b);
+            tma_load_3d(st + S::off_u + j * S::BLK, &maps.u, &bar[s], t0 + 8 * j, it.d0, it.b);
+            tma_load_3d(st + S::off_d + j * S::BLK, &maps.d, &bar[s], t0 + 8 * j, it.d0, it.b);
+            if (MODE == 0 && HAS_Z) tma_load_3d(st + S::off_z + j * S::BLK, &maps.z, &bar[s], t0 + 8 * j, it.d0, it.b);
         }
-        tma_load_3d(st + S::off_B, &maps.B, &bar[buf], t0, 0, b);
-        if (MODE == 0) tma_load_3d(st + S::off_C, &maps.C, &bar[buf], t0, 0, b);
+        tma_load_3d(st + S::off_B, &maps.B, &bar[s], t0, 0, it.b);
+        if (MODE == 0) tma_load_3d(st + S::off_C, &maps.C, &bar[s], t0, 0, it.b);
     };
     // Plain loads for shapes TMA cannot describe (row pitch not a multiple of 16 B).
-    auto generic_loads = [&](int tile, int buf) {
-        const int t0 = t_begin + tile * TT;
-        unsigned char *st = stage(buf);
+    auto generic_loads = [&](const Item &it, int tile, int s) {
+        const int t0 = it.t_begin + tile * kTT;
+        unsigned char *st = stage(s);
         T *us = reinterpret_cast<T *>(st + S::off_u), *ds = reinterpret_cast<T *>(st + S::off_d);
         T *zs = reinterpret_cast<T *>(st + S::off_z);
         const T *gu = static_cast<const T *>(a.u), *gdl = static_cast<const T *>(a.delta);
         const T *gz = static_cast<const T *>(a.z);
-        for (int i = lane; i < kCH * TT; i += kCH) {
-            const int tt = i / kCH, cc = i % kCH, dch = d0 + cc, t = t0 + tt;
+        for (int i = lane; i < CPW * kTT; i += 32) {
+            const int tt = i / CPW, cc = i % CPW, dch = it.d0 + cc, t = t0 + tt;
             const bool in = dch < D && t < L;
-            const size_t off = ((size_t)b * D + dch) * L + t;
-            const int si = (tt / 8) * (kCH * 8) + cc * 8 + (tt % 8);
+            const size_t off = ((size_t)it.b * D + dch) * L + t;
+            const int si = (tt / 8) * (CPW * 8) + cc * 8 + (tt % 8);
             us[si] = in ? gu[off] : T(0.f);
             ds[si] = in ? gdl[off] : T(0.f);
             if (MODE == 0 && HAS_Z) zs[si] = in ? gz[off] : T(0.f);
         }
         T *Bs = reinterpret_cast<T *>(st + S::off_B), *Cs = reinterpret_cast<T *>(st + S::off_C);
         const T *gB = static_cast<const T *>(a.B), *gC = static_cast<const T *>(a.C);
-        for (int i = lane; i < N * TT; i += kCH) {
-            const int n = i / TT, tt = i % TT, t = t0 + tt;
+        for (int i = lane; i < N * kTT; i += 32) {
+            const int n = i / kTT, tt = i % kTT, t = t0 + tt;
             const bool in = t < L;
-            const size_t off = ((size_t)b * N + n) * L + t;
+            const size_t off = ((size_t)it.b * N + n) * L + t;
             Bs[i] = in ? gB[off] : T(0.f);
             if (MODE == 0) Cs[i] = in ? gC[off] : T(0.f);
         }
     };
 
-    if (TMA && lane == 0 && ntiles > 0) issue_loads(0, 0);
+    int cur = grab();
+    if (cur >= items) return;
+    int nxt = grab();
+    Item it = item_of(cur);
+    int s = 0;                 // stage holding the current tile
+    uint32_t phase = 0;        // bit s: parity of stage s's next completion
+    int ostage = 0;            // y tile being written
+    if (TMA) {
+        if (lane == 0) issue_loads(it, 0, 0);
+    }
+    bool failed = false;
 
-    float dsum = 0.f;  // Σ Δ over the chunk (MODE 1)
-
-    for (int tile = 0; tile < ntiles; ++tile) {
-        const int buf = tile & 1;
-        const int t0 = t_begin + tile * TT;
-        unsigned char *st = stage(buf);
-        if (TMA) {
-            const bool ok = mbar_wait_bounded(&bar[buf], (tile >> 1) & 1, kWaitLimit);
-            if (__any_sync(0xffffffffu, !ok)) {
-                record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
-                if (lane == 0) bulk_wait0();
-                return;
+    while (true) {
+        // ---- item set-up: this lane's channel, its A row, bias, skip, start state
+        const int d = it.d0 + c;
+        const bool live = d < D;
+        float2 A2[NQ], h[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            float av[2] = {0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int n = SPT * g + 2 * q + j;
+                if (live && n < N) av[j] = a.A[(size_t)d * N + n] * kLog2e;
             }
-            if (lane == 0 && tile + 1 < ntiles) {
-                fence_proxy_async_smem();
-                issue_loads(tile + 1, buf ^ 1);
-            }
-        } else {
-            generic_loads(tile, buf);
-            __syncwarp();
+            A2[q] = make_float2(av[0], av[1]);
+            h[q] = make_float2(0.f, 0.f);
         }
-
-        // ---- B (and C) widened to fp32, token-major rows, in 4 × 4 blocks
-        {
-            constexpr int NB = SPT / 4, TB = TT / 4;
-            constexpr int UNITS = (MODE == 0 ? 2 : 1) * NB * TB;
-            const T *Bs = reinterpret_cast<const T *>(st + S::off_B);
-            const T *Cs = reinterpret_cast<const T *>(st + S::off_C);
-            for (int it = lane; it < UNITS; it += kCH) {
-                const int mat = it / (NB * TB), r = it % (NB * TB);
-                const int nb = r / TB, tb = r % TB;
-                const T *src = mat ? Cs : Bs;
-                float *dst = mat ? Cf : Bf;
-                float4 v[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int n = 4 * nb + i;
-                    v[i] = n < N ? IO<T>::load4(src + n * TT + 4 * tb) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float bias = (live && a.bias) ? a.bias[d] : 0.f;
+        const float skip = (live && a.Dskip) ? a.Dskip[d] : 0.f;
+        if (MODE == 0) {
+            const float *src = nullptr;
+            bool cg = false;  // read through L2 only: another SM wrote it during this launch
+            if (it.k == 0) {
+                src = a.h0 ? a.h0 + ((size_t)it.b * D + d) * N : nullptr;
+            } else if (chained) {
+                if (lane == 0) {
+                    int polls = 0;
+                    while (ld_acquire(a.flags + it.grp) < it.k && ++polls < kFlagLimit) __nanosleep(64);
+                    if (polls >= kFlagLimit) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
                 }
-                float *row = dst + (4 * tb) * S::BCP + 4 * nb;
-                *reinterpret_cast<float4 *>(row) = make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
-                *reinterpret_cast<float4 *>(row + S::BCP) = make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
-                *reinterpret_cast<float4 *>(row + 2 * S::BCP) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
-                *reinterpret_cast<float4 *>(row + 3 * S::BCP) = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+                __syncwarp();
+                (void)ld_acquire(a.flags + it.grp);  // every lane orders its reads after the hand-off
+                src = a.carry + ((size_t)it.b * D + d) * N;
+                cg = true;
+            } else {
+                src = a.carry + (((size_t)it.b * D + d) * K + it.k) * N;
+                cg = true;
             }
-        }
-        // The y tile written two tiles ago must have left shared memory.
-        if (TMA && MODE == 0 && lane == 0) bulk_wait_read1();
-        __syncwarp();
-
-        T *out = reinterpret_cast<T *>(smem + S::off_out + buf * S::OUT);
-        const T *u_t = reinterpret_cast<const T *>(st + S::off_u);
-        const T *d_t = reinterpret_cast<const T *>(st + S::off_d);
-        const T *z_t = reinterpret_cast<const T *>(st + S::off_z);
-#pragma unroll 1
-        for (int blk = 0; blk < NB8; ++blk) {
-            // ---- per-token terms of this lane's 8 tokens, two tokens per packed op
-            const int eo = blk * (kCH * 8) + lane * 8;
-            float uf[8], df[8], zf[8];
-            IO<T>::load8(u_t + eo, uf);
-            IO<T>::load8(d_t + eo, df);
-            if (MODE == 0 && HAS_Z) IO<T>::load8(z_t + eo, zf);
-            const int valid = t_end - (t0 + 8 * blk);  // tokens of this block inside the chunk
-            float2 dl[4], du[4], gt[4], dug[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float2 x = __fadd2_rn(make_float2(df[2 * j], df[2 * j + 1]), make_float2(bias, bias));
-                if (a.delta_softplus) x = make_float2(IO<T>::softplus(x.x), IO<T>::softplus(x.y));
-                if (valid < 8) {  // Δ = 0 keeps the state: Ā = 1, B̄u = 0
-                    if (2 * j >= valid) x.x = 0.f;
-                    if (2 * j + 1 >= valid) x.y = 0.f;
-                }
-                const float2 uu = make_float2(uf[2 * j], uf[2 * j + 1]);
-                dl[j] = x;
-                du[j] = __fmul2_rn(x, uu);
-                if (MODE == 0) {
-                    gt[j] = HAS_Z ? gate2<T>(make_float2(zf[2 * j], zf[2 * j + 1])) : make_float2(1.f, 1.f);
-                    dug[j] = __fmul2_rn(__fmul2_rn(make_float2(skip, skip), uu), gt[j]);
-                }
-            }
-            // ---- the recurrence over the block's 8 tokens, all SPT states.  The
-            // decays Ā and inputs B̄u of token j+1 are formed before the state of
-            // token j is updated, so the exponentials overlap the FMA chain.
-            float2 an[NQ], bn[NQ];
-            auto decay_input = [&](int j, float2 *ao, float2 *bo) {
-                const float dv = (j & 1) ? dl[j >> 1].y : dl[j >> 1].x;
-                const float uv = (j & 1) ? du[j >> 1].y : du[j >> 1].x;
-                const float2 d2 = make_float2(dv, dv), du2 = make_float2(uv, uv);
-                const float *Brow = Bf + (8 * blk + j) * S::BCP;
-#pragma unroll
-                for (int q4 = 0; q4 < SPT / 4; ++q4) {
-                    const float4 bq = *reinterpret_cast<const float4 *>(Brow + 4 * q4);
-                    const float2 x0 = __fmul2_rn(d2, A2[2 * q4]);
-                    const float2 x1 = __fmul2_rn(d2, A2[2 * q4 + 1]);
-                    ao[2 * q4] = make_float2(ex2(x0.x), ex2(x0.y));
-                    ao[2 * q4 + 1] = make_float2(ex2(x1.x), ex2(x1.y));
-                    bo[2 * q4] = __fmul2_rn(make_float2(bq.x, bq.y), du2);
-                    bo[2 * q4 + 1] = __fmul2_rn(make_float2(bq.z, bq.w), du2);
-                }
-            };
-            decay_input(0, an, bn);
-            float y[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float2 ac[NQ], bc[NQ];
+            if (src && live) {
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) {
-                    ac[q] = an[q];
-                    bc[q] = bn[q];
+                    const int n = SPT * g + 2 * q;
+                    float hx = 0.f, hy = 0.f;
+                    if (n < N) hx = cg ? __ldcg(src + n) : src[n];
+                    if (n + 1 < N) hy = cg ? __ldcg(src + n + 1) : src[n + 1];
+                    h[q] = make_float2(hx, hy);
                 }
-                if (j < 7) decay_input(j + 1, an, bn);
-                const float *Crow = Cf + (8 * blk + j) * S::BCP;
-                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+            }
+        }
+        float dsum = 0.f;  // Σ Δ over the chunk (MODE 1)
+
+        for (int tile = 0; tile < it.ntiles; ++tile) {
+            const int t0 = it.t_begin + tile * kTT;
+            unsigned char *st = stage(s);
+            if (TMA) {
+                const bool ok = mbar_wait_bounded(&bar[s], (phase >> s) & 1, kWaitLimit);
+                phase ^= 1u << s;
+                if (__any_sync(FULL, !ok)) {
+                    failed = true;
+                    break;
+                }
+                // Next tile: of this item, else the first tile of the next item.
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    if (tile + 1 < it.ntiles) issue_loads(it, tile + 1, s ^ 1);
+                    else if (nxt < items) issue_loads(item_of(nxt), 0, s ^ 1);
+                }
+            } else {
+                generic_loads(it, tile, s);
+                __syncwarp();
+            }
+
+            // ---- B (and C) widened to fp32, token-major rows, in 4 × 4 blocks
+            {
+                constexpr int NB = S::NP / 4, TB = kTT / 4;
+                constexpr int UNITS = (MODE == 0 ? 2 : 1) * NB * TB;
+                const T *Bs = reinterpret_cast<const T *>(st + S::off_B);
+                const T *Cs = reinterpret_cast<const T *>(st + S::off_C);
+                for (int u = lane; u < UNITS; u += 32) {
+                    const int mat = u / (NB * TB), r = u % (NB * TB);
+                    const int nb = r / TB, tb = r % TB;
+                    const T *src = mat ? Cs : Bs;
+                    float *dst = mat ? Cf : Bf;
+                    float4 v[4];
 #pragma unroll
-                for (int q4 = 0; q4 < SPT / 4; ++q4) {
-                    h[2 * q4] = __ffma2_rn(ac[2 * q4], h[2 * q4], bc[2 * q4]);
-                    h[2 * q4 + 1] = __ffma2_rn(ac[2 * q4 + 1], h[2 * q4 + 1], bc[2 * q4 + 1]);
-                    if (MODE == 0) {
-                        const float4 cq = *reinterpret_cast<const float4 *>(Crow + 4 * q4);
-                        if (q4 == 0) {
-                            acc0 = __fmul2_rn(make_float2(cq.x, cq.y), h[0]);
-                            acc1 = __fmul2_rn(make_float2(cq.z, cq.w), h[1]);
+                    for (int i = 0; i < 4; ++i) {
+                        const int n = 4 * nb + i;
+                        v[i] = n < N ? IO<T>::load4(src + n * kTT + 4 * tb) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    float *row = dst + (4 * tb) * S::BCP + 4 * nb;
+                    *reinterpret_cast<float4 *>(row) = make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
+                    *reinterpret_cast<float4 *>(row + S::BCP) = make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
+                    *reinterpret_cast<float4 *>(row + 2 * S::BCP) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
+                    *reinterpret_cast<float4 *>(row + 3 * S::BCP) = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+                }
+            }
+            // The y tile written two tiles ago must have left shared memory.
+            if (TMA && MODE == 0 && lane == 0) bulk_wait_read1();
+            __syncwarp();
+
+            T *out = reinterpret_cast<T *>(smem + S::off_out + ostage * S::OUT);
+            const T *u_t = reinterpret_cast<const T *>(st + S::off_u);
+            const T *d_t = reinterpret_cast<const T *>(st + S::off_d);
+            const T *z_t = reinterpret_cast<const T *>(st + S::off_z);
+#pragma unroll 1
+            for (int blk = 0; blk < NB8; ++blk) {
+                // ---- per-token terms of the channel's 8 tokens (both lanes of a
+                // channel form Δ and Δ·u; the gate only for the tokens they output)
+                const int eo = blk * (CPW * 8) + c * 8;
+                float uf[8], df[8], zf[8];
+                IO<T>::load8(u_t + eo, uf);
+                IO<T>::load8(d_t + eo, df);
+                if (MODE == 0 && HAS_Z) IO<T>::load8(z_t + eo, zf);
+                const int valid = it.t_end - (t0 + 8 * blk);  // tokens of this block inside the chunk
+                float2 dl[4], du[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float2 x = __fadd2_rn(make_float2(df[2 * j], df[2 * j + 1]), make_float2(bias, bias));
+                    if (a.delta_softplus) x = make_float2(IO<T>::softplus(x.x), IO<T>::softplus(x.y));
+                    if (valid < 8) {  // Δ = 0 keeps the state: Ā = 1, B̄u = 0
+                        if (2 * j >= valid) x.x = 0.f;
+                        if (2 * j + 1 >= valid) x.y = 0.f;
+                    }
+                    dl[j] = x;
+                    du[j] = __fmul2_rn(x, make_float2(uf[2 * j], uf[2 * j + 1]));
+                }
+                // Gate and D·u·gate for the token pairs this lane outputs:
+                // NG = 1: all four pairs; NG = 2: pairs 2m + g of each half.
+                constexpr int OP = NG == 1 ? 4 : 2;
+                float2 gt[OP], dug[OP];
+                if (MODE == 0) {
+#pragma unroll
+                    for (int m = 0; m < OP; ++m) {
+                        const int j0 = NG == 1 ? 2 * m : 4 * m;  // first token of the pair when g = 0
+                        float2 zz = make_float2(1.f, 1.f), uu;
+                        if (NG == 1) {
+                            uu = make_float2(uf[j0], uf[j0 + 1]);
+                            if (HAS_Z) zz = make_float2(zf[j0], zf[j0 + 1]);
                         } else {
-                            acc0 = __ffma2_rn(make_float2(cq.x, cq.y), h[2 * q4], acc0);
-                            acc1 = __ffma2_rn(make_float2(cq.z, cq.w), h[2 * q4 + 1], acc1);
+                            uu = g ? make_float2(uf[j0 + 2], uf[j0 + 3]) : make_float2(uf[j0], uf[j0 + 1]);
+                            if (HAS_Z) zz = g ? make_float2(zf[j0 + 2], zf[j0 + 3]) : make_float2(zf[j0], zf[j0 + 1]);
                         }
+                        gt[m] = HAS_Z ? gate2<T>(zz) : make_float2(1.f, 1.f);
+                        dug[m] = __fmul2_rn(__fmul2_rn(make_float2(skip, skip), uu), gt[m]);
+                    }
+                }
+                // ---- the recurrence over the block's 8 tokens.  Ā and B̄u of
+                // token j+1 are formed before the state of token j is updated.
+                float2 an[NQ], bn[NQ];
+                auto decay_input = [&](int j, float2 *ao, float2 *bo) {
+                    const float dv = (j & 1) ? dl[j >> 1].y : dl[j >> 1].x;
+                    const float uv = (j & 1) ? du[j >> 1].y : du[j >> 1].x;
+                    const float2 d2 = make_float2(dv, dv), du2 = make_float2(uv, uv);
+                    const float *Brow = Bf + (8 * blk + j) * S::BCP + SPT * g;
+#pragma unroll
+                    for (int q4 = 0; q4 < SPT / 4; ++q4) {
+                        const float4 bq = *reinterpret_cast<const float4 *>(Brow + 4 * q4);
+                        const float2 x0 = __fmul2_rn(d2, A2[2 * q4]);
+                        const float2 x1 = __fmul2_rn(d2, A2[2 * q4 + 1]);
+                        ao[2 * q4] = make_float2(ex2(x0.x), ex2(x0.y));
+                        ao[2 * q4 + 1] = make_float2(ex2(x1.x), ex2(x1.y));
+                        bo[2 * q4] = __fmul2_rn(make_float2(bq.x, bq.y), du2);
+                        bo[2 * q4 + 1] = __fmul2_rn(make_float2(bq.z, bq.w), du2);
+                    }
+                };
+                decay_input(0, an, bn);
+                float p[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float2 ac[NQ], bc[NQ];
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) {
+                        ac[q] = an[q];
+                        bc[q] = bn[q];
+                    }
+                    if (j < 7) decay_input(j + 1, an, bn);
+                    const float *Crow = Cf + (8 * blk + j) * S::BCP + SPT * g;
+                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int q4 = 0; q4 < SPT / 4; ++q4) {
+                        h[2 * q4] = __ffma2_rn(ac[2 * q4], h[2 * q4], bc[2 * q4]);
+                        h[2 * q4 + 1] = __ffma2_rn(ac[2 * q4 + 1], h[2 * q4 + 1], bc[2 * q4 + 1]);
+                        if (MODE == 0) {
+                            const float4 cq = *reinterpret_cast<const float4 *>(Crow + 4 * q4);
+                            if (q4 == 0) {
+                                acc0 = __fmul2_rn(make_float2(cq.x, cq.y), h[0]);
+                                acc1 = __fmul2_rn(make_float2(cq.z, cq.w), h[1]);
+                            } else {
+                                acc0 = __ffma2_rn(make_float2(cq.x, cq.y), h[2 * q4], acc0);
+                                acc1 = __ffma2_rn(make_float2(cq.z, cq.w), h[2 * q4 + 1], acc1);
+                            }
+                        }
+                    }
+                    if (MODE == 0) {
+                        const float2 s2 = __fadd2_rn(acc0, acc1);
+                        p[j] = s2.x + s2.y;
+                    } else {
+                        dsum += (j & 1) ? dl[j >> 1].y : dl[j >> 1].x;
                     }
                 }
                 if (MODE == 0) {
-                    const float2 s2 = __fadd2_rn(acc0, acc1);
-                    const float g = (j & 1) ? gt[j >> 1].y : gt[j >> 1].x;
-                    const float e = (j & 1) ? dug[j >> 1].y : dug[j >> 1].x;
-                    y[j] = fmaf(s2.x + s2.y, g, e);
-                } else {
-                    dsum += (j & 1) ? dl[j >> 1].y : dl[j >> 1].x;
-                }
-            }
-            if (MODE == 0) Pack8<T>::store(out + eo, y);
-        }
-
-        if (MODE == 0) {
-            if (TMA) {
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
+                    if (NG == 1) {
+                        float y[8];
 #pragma unroll
-                    for (int j = 0; j < NB8; ++j)
-                        tma_store_3d(&maps.y, out + j * (kCH * 8), t0 + 8 * j, d0, b);
-                    bulk_commit();
-                }
-            } else {
-                __syncwarp();
-                T *gy = static_cast<T *>(a.y);
-                for (int i = lane; i < kCH * TT; i += kCH) {
-                    const int tt = i / kCH, cc = i % kCH, dch = d0 + cc, t = t0 + tt;
-                    if (dch < D && t < t_end)
-                        gy[((size_t)b * D + dch) * L + t] = out[(tt / 8) * (kCH * 8) + cc * 8 + (tt % 8)];
+                        for (int m = 0; m < 4; ++m) {
+                            const float2 y2 = __ffma2_rn(make_float2(p[2 * m], p[2 * m + 1]), gt[m], dug[m]);
+                            y[2 * m] = y2.x;
+                            y[2 * m + 1] = y2.y;
+                        }
+                        Pack<T>::store8(out + eo, y);
+                    } else {
+                        // Transposed sum over the two lanes of a channel, four
+                        // tokens at a time: lane g keeps tokens 4m + 2g, 4m + 2g + 1.
+#pragma unroll
+                        for (int m = 0; m < 2; ++m) {
+                            const float k0 = g ? p[4 * m + 2] : p[4 * m], k1 = g ? p[4 * m + 3] : p[4 * m + 1];
+                            const float s0 = g ? p[4 * m] : p[4 * m + 2], s1 = g ? p[4 * m + 1] : p[4 * m + 3];
+                            const float r0 = __shfl_xor_sync(FULL, s0, 1), r1 = __shfl_xor_sync(FULL, s1, 1);
+                            const float2 y2 = __ffma2_rn(__fadd2_rn(make_float2(k0, k1), make_float2(r0, r1)), gt[m], dug[m]);
+                            Pack<T>::store2(out + eo + 4 * m + 2 * g, y2);
+                        }
+                    }
                 }
             }
-        }
-        __syncwarp();  // this tile's B/C rows and raw stage are free again
-    }
-    if (TMA && MODE == 0 && lane == 0) bulk_wait0();
 
-    if (MODE == 0) {
-        if (k == a.nchunks - 1 && a.hL && live) {
+            if (MODE == 0) {
+                if (TMA) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int j = 0; j < NB8; ++j)
+                            tma_store_3d(&maps.y, out + j * (CPW * 8), t0 + 8 * j, it.d0, it.b);
+                        bulk_commit();
+                    }
+                } else {
+                    __syncwarp();
+                    T *gy = static_cast<T *>(a.y);
+                    for (int i = lane; i < CPW * kTT; i += 32) {
+                        const int tt = i / CPW, cc = i % CPW, dch = it.d0 + cc, t = t0 + tt;
+                        if (dch < D && t < it.t_end)
+                            gy[((size_t)it.b * D + dch) * L + t] = out[(tt / 8) * (CPW * 8) + cc * 8 + (tt % 8)];
+                    }
+                }
+                ostage ^= 1;
+            }
+            __syncwarp();  // this tile's B/C rows and stage are free again
+            s ^= 1;
+        }
+        if (failed) break;
+
+        // ---- item end: hand the state on, or write the final state / aggregate
+        if (MODE == 0) {
+            float *dst = nullptr;
+            const bool last = it.k == K - 1;
+            if (last) dst = a.hL ? a.hL + ((size_t)it.b * D + d) * N : nullptr;
+            else if (chained) dst = a.carry + ((size_t)it.b * D + d) * N;
+            if (dst && live) {
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const int n = SPT * g + 2 * q;
+                    if (n < N) dst[n] = h[q].x;
+                    if (n + 1 < N) dst[n + 1] = h[q].y;
+                }
+            }
+            if (chained && !last) {
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release(a.flags + it.grp, it.k + 1);
+            }
+        } else if (live) {
 #pragma unroll
             for (int q = 0; q < NQ; ++q) {
-                const int n = 2 * q;
-                if (n < N) a.hL[((size_t)b * D + d) * N + n] = h[q].x;
-                if (n + 1 < N) a.hL[((size_t)b * D + d) * N + n + 1] = h[q].y;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int n = SPT * g + 2 * q + j;
+                    const float av = j ? A2[q].y : A2[q].x;
+                    const float hv = j ? h[q].y : h[q].x;
+                    if (n < N)
+                        a.agg[(((size_t)it.b * D + d) * (K - 1) + it.k) * N + n] = make_float2(ex2(av * dsum), hv);
+                }
             }
         }
-    } else if (live) {
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int n = 2 * q + j;
-                const float av = j ? A2[q].y : A2[q].x;
-                const float hv = j ? h[q].y : h[q].x;
-                if (n < N)
-                    a.agg[(((size_t)b * D + d) * (a.nchunks - 1) + k) * N + n] = make_float2(ex2(av * dsum), hv);
-            }
-        }
+
+        cur = nxt;
+        if (cur >= items) break;
+        nxt = grab();
+        it = item_of(cur);
     }
+    if (failed) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
+    if (TMA && MODE == 0 && lane == 0) bulk_wait0();
 }
 
-// Chains the chunk aggregates from h0: carry[0] = h0 and
+// Chains the chunk aggregates from h0 (two-pass mode): carry[0] = h0 and
 // carry[k+1] = P_k · carry[k] + S_k, the state chunk k+1 starts from.
 // One thread per (b, d, n).
 __global__ void carry_kernel(const ScanArgs a) {
@@ -440,73 +569,99 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, size_t es, const void *ptr
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int SPT, bool HAS_Z, bool TMA, int MODE>
-cudaError_t launch_one(const Maps &maps, const ScanArgs &a, dim3 grid, cudaStream_t st) {
-    using S = WTile<T, SPT, kTT>;
-    auto kern = scan_kernel<T, SPT, kTT, HAS_Z, TMA, MODE>;
-    static bool attr_set = false;
-    if (!attr_set) {
+// Lanes per channel and states per lane for a state size N.
+struct Split {
+    int spt, ng;
+};
+Split split_for(int64_t dstate) {
+    if (dstate <= 4) return {4, 1};
+    if (dstate <= 8) return {8, 1};
+    return {8, 2};
+}
+
+template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, int MODE>
+cudaError_t launch_one(const Maps &maps, const ScanArgs &a, int items, cudaStream_t st) {
+    using S = WTile<T, SPT, NG>;
+    auto kern = scan_kernel<T, SPT, NG, HAS_Z, TMA, MODE>;
+    static int per_sm = 0;  // resident warps per SM for this instantiation
+    if (per_sm == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::bytes);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32, S::bytes);
+        if (e != cudaSuccess) return e;
+        per_sm = std::max(1, std::min(n, kWarpsPerSM));
     }
-    kern<<<grid, kCH, S::bytes, st>>>(maps, a);
+    int sms = kSMs;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = std::max(1, std::min(items, sms * per_sm));
+    kern<<<grid, 32, S::bytes, st>>>(maps, a);
     return cudaGetLastError();
 }
 
-template <typename T, int SPT, bool HAS_Z, bool TMA>
+template <typename T, int SPT, int NG, bool HAS_Z, bool TMA>
 cudaError_t launch_all(const Maps &maps, const ScanArgs &a, cudaStream_t st) {
-    const unsigned gx = (unsigned)((a.dim + kCH - 1) / kCH);
     cudaError_t e;
-    if (a.nchunks > 1) {
-        e = launch_one<T, SPT, false, TMA, 1>(maps, a, dim3(gx, a.batch, a.nchunks - 1), st);
+    if (a.nchunks > 1 && !a.chained) {
+        e = launch_one<T, SPT, NG, false, TMA, 1>(maps, a, a.groups * (a.nchunks - 1), st);
         if (e != cudaSuccess) return e;
         const size_t total = (size_t)a.batch * a.dim * a.dstate;
         carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    return launch_one<T, SPT, HAS_Z, TMA, 0>(maps, a, dim3(gx, a.batch, a.nchunks), st);
+    return launch_one<T, SPT, NG, HAS_Z, TMA, 0>(maps, a, a.groups * a.nchunks, st);
 }
 
-template <typename T, int SPT>
+template <typename T, int SPT, int NG>
 cudaError_t dispatch_z_tma(const Maps &maps, const ScanArgs &a, bool tma, cudaStream_t st) {
     const bool z = a.z != nullptr;
-    if (tma) return z ? launch_all<T, SPT, true, true>(maps, a, st) : launch_all<T, SPT, false, true>(maps, a, st);
-    return z ? launch_all<T, SPT, true, false>(maps, a, st) : launch_all<T, SPT, false, false>(maps, a, st);
+    if (tma)
+        return z ? launch_all<T, SPT, NG, true, true>(maps, a, st) : launch_all<T, SPT, NG, false, true>(maps, a, st);
+    return z ? launch_all<T, SPT, NG, true, false>(maps, a, st) : launch_all<T, SPT, NG, false, false>(maps, a, st);
 }
 
-// States held per lane: N rounded up to 4, 8 or 16.
-int spt_for(int64_t dstate) { return dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16); }
-
 template <typename T>
-cudaError_t dispatch_spt(const Maps &maps, const ScanArgs &a, bool tma, cudaStream_t st) {
-    switch (spt_for(a.dstate)) {
-        case 4: return dispatch_z_tma<T, 4>(maps, a, tma, st);
-        case 8: return dispatch_z_tma<T, 8>(maps, a, tma, st);
-        default: return dispatch_z_tma<T, 16>(maps, a, tma, st);
-    }
+cudaError_t dispatch_split(const Maps &maps, const ScanArgs &a, Split sp, bool tma, cudaStream_t st) {
+    if (sp.spt == 4) return dispatch_z_tma<T, 4, 1>(maps, a, tma, st);
+    if (sp.ng == 1) return dispatch_z_tma<T, 8, 1>(maps, a, tma, st);
+    return dispatch_z_tma<T, 8, 2>(maps, a, tma, st);
 }
 
 }  // namespace
 
 int scan_groups(int64_t dstate) { return dstate <= 4 ? 1 : (dstate <= 8 ? 2 : 4); }
 
-int64_t scan_chunk_len(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t requested) {
-    (void)dstate;
-    if (requested > 0) return std::min<int64_t>(requested, ((seqlen + 63) / 64) * 64);
-    // One lane per channel: split the sequence until there is at least one
-    // warp per scheduler (148 SMs × 4), since each chunk beyond the first costs
-    // an extra aggregate pass.
-    const int64_t threads = batch * dim;
-    const int64_t want = 148LL * 4 * 32;
-    int64_t K = (want + threads - 1) / threads;
-    K = std::max<int64_t>(1, std::min<int64_t>(K, (seqlen + 511) / 512));
-    const int64_t len = (seqlen + K - 1) / K;
-    return ((len + 63) / 64) * 64;
+ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t requested) {
+    ScanPlan p;
+    const Split sp = split_for(dstate);
+    p.cpw = 32 / sp.ng;
+    p.groups = batch * ((dim + p.cpw - 1) / p.cpw);
+    const int64_t resident = (int64_t)kSMs * kWarpsPerSM;
+    const int64_t Lr = ((seqlen + 63) / 64) * 64;
+    // Chained when the groups alone fill the resident warps (a two-pass split
+    // would add an aggregate pass for parallelism the GPU does not need).
+    p.chained = p.groups * 4 >= resident * 3;
+    if (p.chained) {
+        p.chunk_len = requested > 0 ? std::min<int64_t>(requested, Lr) : std::min<int64_t>(kDefaultChunk, Lr);
+    } else if (requested > 0) {
+        p.chunk_len = std::min<int64_t>(requested, Lr);
+    } else {
+        // Split the sequence until the items fill the resident warps.
+        int64_t K = (resident + p.groups - 1) / p.groups;
+        K = std::max<int64_t>(1, std::min<int64_t>(K, (seqlen + 511) / 512));
+        const int64_t len = (seqlen + K - 1) / K;
+        p.chunk_len = ((len + 63) / 64) * 64;
+    }
+    p.nchunks = (seqlen + p.chunk_len - 1) / p.chunk_len;
+    if (p.nchunks == 1) p.chained = false;
+    return p;
 }
 
 cudaError_t scan_launch(const ScanArgs &a, bool bf16, cudaStream_t st) {
+    const Split sp = split_for(a.dstate);
+    const int cpw = 32 / sp.ng;
     const size_t es = bf16 ? 2 : 4;
     // TMA needs a row pitch that is a multiple of 16 bytes.
     const bool tma = ((size_t)a.seqlen * es) % 16 == 0;
@@ -514,15 +669,15 @@ cudaError_t scan_launch(const ScanArgs &a, bool bf16, cudaStream_t st) {
     memset(&maps, 0, sizeof(maps));
     if (tma) {
         const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-        bool ok = make_map(&maps.u, dt, es, a.u, a.seqlen, a.dim, a.batch, 8, kCH) &&
-                  make_map(&maps.d, dt, es, a.delta, a.seqlen, a.dim, a.batch, 8, kCH) &&
+        bool ok = make_map(&maps.u, dt, es, a.u, a.seqlen, a.dim, a.batch, 8, cpw) &&
+                  make_map(&maps.d, dt, es, a.delta, a.seqlen, a.dim, a.batch, 8, cpw) &&
                   make_map(&maps.B, dt, es, a.B, a.seqlen, a.dstate, a.batch, kTT, a.dstate) &&
                   make_map(&maps.C, dt, es, a.C, a.seqlen, a.dstate, a.batch, kTT, a.dstate) &&
-                  make_map(&maps.y, dt, es, a.y, a.seqlen, a.dim, a.batch, 8, kCH);
-        if (ok && a.z) ok = make_map(&maps.z, dt, es, a.z, a.seqlen, a.dim, a.batch, 8, kCH);
+                  make_map(&maps.y, dt, es, a.y, a.seqlen, a.dim, a.batch, 8, cpw);
+        if (ok && a.z) ok = make_map(&maps.z, dt, es, a.z, a.seqlen, a.dim, a.batch, 8, cpw);
         if (!ok) return cudaErrorInvalidValue;
     }
-    return bf16 ? dispatch_spt<__nv_bfloat16>(maps, a, tma, st) : dispatch_spt<float>(maps, a, tma, st);
+    return bf16 ? dispatch_split<__nv_bfloat16>(maps, a, sp, tma, st) : dispatch_split<float>(maps, a, sp, tma, st);
 }
 
 }  // namespace ssm

@@ -15,11 +15,28 @@ struct ScanArgs {
     const float *h0;
     void *y;
     float *hL;
-    float2 *agg;     // [b][D][K-1][N] (Π Ā, h_end from zero) per chunk
-    float *carry;    // [b][D][K][N] state entering chunk k
+    float2 *agg;     // two-pass mode: [b][D][K-1][N] (Π Ā, h_end from zero) per chunk
+    float *carry;    // two-pass: [b][D][K][N] state entering chunk k; chained: [b][D][N] hand-off
     int *status;     // device status word (0 = ok)
+    int *tickets;    // two work counters (main pass, aggregate pass), zero at launch
+    int *flags;      // chained mode: chunks finished per channel group, zero at launch
     int chunk_len;   // tokens per chunk (multiple of 64)
     int nchunks;     // K
+    int groups;      // channel groups: batch × ceil(dim / channels per warp)
+    int chained;     // 1: chunk k waits for chunk k-1's state; 0: two-pass carries
+};
+
+// How a scan is cut into work items.  One warp owns a group of channels for
+// one chunk of the sequence.  Chained: the chunks of a group run in order,
+// each taking the previous one's final state (enough groups to fill the GPU).
+// Two-pass: an aggregate pass and a carry pass precompute every chunk's
+// starting state so that all chunks run at once (few groups, long sequences).
+struct ScanPlan {
+    int cpw;            // channels per warp
+    int64_t groups;     // batch × ceil(dim / cpw)
+    bool chained;
+    int64_t chunk_len;  // multiple of 64
+    int64_t nchunks;
 };
 
 struct StepArgs {
@@ -32,7 +49,7 @@ struct StepArgs {
 };
 
 int scan_groups(int64_t dstate);
-int64_t scan_chunk_len(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t requested);
+ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t requested);
 cudaError_t scan_launch(const ScanArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t step_launch(const StepArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t mufu_ex2_launch(float *sink, int blocks, int iters, cudaStream_t stream);

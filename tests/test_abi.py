@@ -101,7 +101,14 @@ def test_workspace_size():
     # the small-model layer shape is split into chunks automatically
     p = valid_scan(batch=2, dim=1536, seqlen=2048)
     assert capi.ssm_scan_workspace_size(p) > 256
+    # enough channel groups to fill the GPU: chunks are chained, and the
+    # workspace holds one flag per group of 16 channels and one hand-off state
     p = valid_scan(batch=4, dim=5120, seqlen=2048)
+    groups = 4 * 5120 // 16
+    flags = -(-groups * 4 // 256) * 256
+    assert capi.ssm_scan_workspace_size(p) == 256 + flags + 4 * 5120 * 16 * 4
+    # a single chunk needs the header only
+    p = valid_scan(batch=1, dim=64, seqlen=256)
     assert capi.ssm_scan_workspace_size(p) == 256
     # too small a workspace is rejected
     p = valid_scan(chunk_len=64, workspace_bytes=300)
