@@ -42,8 +42,15 @@
 
 namespace ssm {
 
+#ifndef SSM_SCAN_N16_LANES
+#define SSM_SCAN_N16_LANES 2
+#endif
+#ifndef SSM_SCAN_WARPS_PER_SM
+#define SSM_SCAN_WARPS_PER_SM 8
+#endif
+
 constexpr int kTT = 32;                // tokens per tile (chunks are multiples of 64)
-constexpr int kWarpsPerSM = 8;         // resident warps targeted per SM (2 per scheduler)
+constexpr int kWarpsPerSM = SSM_SCAN_WARPS_PER_SM;  // resident warps targeted per SM
 constexpr int kSMs = 148;              // B300
 constexpr int kWaitLimit = 1 << 22;    // mbarrier polls before giving up
 constexpr int kFlagLimit = 1 << 24;    // polls of a predecessor's flag before giving up
@@ -386,7 +393,27 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     }
                 };
                 decay_input(0, an, bn);
+                // The read-out C·h of token j runs after the state update of
+                // token j + 1, so the two chains interleave.
                 float p[8];
+                float2 hp[NQ];
+                auto readout = [&](int j, const float2 *hs) {
+                    const float *Crow = Cf + (8 * blk + j) * S::BCP + SPT * g;
+                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int q4 = 0; q4 < SPT / 4; ++q4) {
+                        const float4 cq = *reinterpret_cast<const float4 *>(Crow + 4 * q4);
+                        if (q4 == 0) {
+                            acc0 = __fmul2_rn(make_float2(cq.x, cq.y), hs[0]);
+                            acc1 = __fmul2_rn(make_float2(cq.z, cq.w), hs[1]);
+                        } else {
+                            acc0 = __ffma2_rn(make_float2(cq.x, cq.y), hs[2 * q4], acc0);
+                            acc1 = __ffma2_rn(make_float2(cq.z, cq.w), hs[2 * q4 + 1], acc1);
+                        }
+                    }
+                    const float2 s2 = __fadd2_rn(acc0, acc1);
+                    p[j] = s2.x + s2.y;
+                };
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     float2 ac[NQ], bc[NQ];
@@ -396,30 +423,17 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                         bc[q] = bn[q];
                     }
                     if (j < 7) decay_input(j + 1, an, bn);
-                    const float *Crow = Cf + (8 * blk + j) * S::BCP + SPT * g;
-                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int q4 = 0; q4 < SPT / 4; ++q4) {
-                        h[2 * q4] = __ffma2_rn(ac[2 * q4], h[2 * q4], bc[2 * q4]);
-                        h[2 * q4 + 1] = __ffma2_rn(ac[2 * q4 + 1], h[2 * q4 + 1], bc[2 * q4 + 1]);
-                        if (MODE == 0) {
-                            const float4 cq = *reinterpret_cast<const float4 *>(Crow + 4 * q4);
-                            if (q4 == 0) {
-                                acc0 = __fmul2_rn(make_float2(cq.x, cq.y), h[0]);
-                                acc1 = __fmul2_rn(make_float2(cq.z, cq.w), h[1]);
-                            } else {
-                                acc0 = __ffma2_rn(make_float2(cq.x, cq.y), h[2 * q4], acc0);
-                                acc1 = __ffma2_rn(make_float2(cq.z, cq.w), h[2 * q4 + 1], acc1);
-                            }
-                        }
-                    }
+                    for (int q = 0; q < NQ; ++q) h[q] = __ffma2_rn(ac[q], h[q], bc[q]);
                     if (MODE == 0) {
-                        const float2 s2 = __fadd2_rn(acc0, acc1);
-                        p[j] = s2.x + s2.y;
+                        if (j > 0) readout(j - 1, hp);
+#pragma unroll
+                        for (int q = 0; q < NQ; ++q) hp[q] = h[q];
                     } else {
                         dsum += (j & 1) ? dl[j >> 1].y : dl[j >> 1].x;
                     }
                 }
+                if (MODE == 0) readout(7, hp);
                 if (MODE == 0) {
                     if (NG == 1) {
                         float y[8];
@@ -486,7 +500,8 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 }
             }
             if (chained && !last) {
-                __threadfence();
+                // The warp barrier orders every lane's state stores before lane
+                // 0's release store; a reader that acquires the flag sees them.
                 __syncwarp();
                 if (lane == 0) st_release(a.flags + it.grp, it.k + 1);
             }
@@ -576,7 +591,7 @@ struct Split {
 Split split_for(int64_t dstate) {
     if (dstate <= 4) return {4, 1};
     if (dstate <= 8) return {8, 1};
-    return {8, 2};
+    return SSM_SCAN_N16_LANES == 1 ? Split{16, 1} : Split{8, 2};
 }
 
 template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, int MODE>
@@ -625,8 +640,12 @@ cudaError_t dispatch_z_tma(const Maps &maps, const ScanArgs &a, bool tma, cudaSt
 template <typename T>
 cudaError_t dispatch_split(const Maps &maps, const ScanArgs &a, Split sp, bool tma, cudaStream_t st) {
     if (sp.spt == 4) return dispatch_z_tma<T, 4, 1>(maps, a, tma, st);
-    if (sp.ng == 1) return dispatch_z_tma<T, 8, 1>(maps, a, tma, st);
+    if (sp.spt == 8 && sp.ng == 1) return dispatch_z_tma<T, 8, 1>(maps, a, tma, st);
+#if SSM_SCAN_N16_LANES == 1
+    return dispatch_z_tma<T, 16, 1>(maps, a, tma, st);
+#else
     return dispatch_z_tma<T, 8, 2>(maps, a, tma, st);
+#endif
 }
 
 }  // namespace
