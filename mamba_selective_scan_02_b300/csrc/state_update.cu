@@ -165,7 +165,200 @@ __global__ void __launch_bounds__(kStepThreads) step_wide_kernel(const StepArgs 
     }
 }
 
+// Decode as a TMA-fed stream (N = 16, D a multiple of 128, 16-byte aligned
+// pointers).  A persistent CTA walks tiles of 128 consecutive channels; per
+// tile one thread moves the 8 KB state tile, the channels' u, Δraw and z, and
+// the sequence's B and C rows into shared memory with cp.async.bulk on an
+// mbarrier, kStreamAhead tiles ahead; a stage is refilled only once the bulk
+// store issued from it two tiles earlier has read it.  The A rows, bias and D,
+// the same for every sequence and resident in L2, are read by the threads
+// themselves one tile ahead.  The 128 threads
+// update the state in place in shared memory (four lanes per channel, one
+// 16-byte word each, conflict-free), and the tile leaves with bulk stores.
+constexpr int kStreamCh = 128;     // channels per tile
+#ifndef SSM_STREAM_STAGES
+#define SSM_STREAM_STAGES 4
+#endif
+constexpr int kStreamStages = SSM_STREAM_STAGES;  // stages in shared memory
+constexpr int kStreamAhead = kStreamStages - 2;   // tiles loading ahead of the one being updated
+
+template <typename T> struct StreamTile {
+    static constexpr int ES = (int)sizeof(T);
+    static constexpr int off_h = 0;                                  // 128 × 16 fp32
+    static constexpr int off_u = off_h + kStreamCh * 64;             // 128 T
+    static constexpr int off_d = off_u + kStreamCh * ES;
+    static constexpr int off_z = off_d + kStreamCh * ES;
+    static constexpr int off_B = off_z + kStreamCh * ES;             // 16 T
+    static constexpr int off_C = off_B + 16 * ES;
+    static constexpr int off_y = off_C + 16 * ES;                    // 128 T
+    static constexpr int bytes = (off_y + kStreamCh * ES + 127) / 128 * 128;
+};
+
+template <typename T, bool HAS_Z>
+__global__ void __launch_bounds__(kStreamCh) step_stream_kernel(const StepArgs a) {
+    using S = StreamTile<T>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kStreamStages * S::bytes);
+    const int tid = threadIdx.x;
+    const int ntiles = (int)((size_t)a.batch * a.dim / kStreamCh);
+    const int tiles_per_seq = a.dim / kStreamCh;
+    const int nmine = ntiles > (int)blockIdx.x ? (ntiles - 1 - (int)blockIdx.x) / gridDim.x + 1 : 0;
+    const T *up = static_cast<const T *>(a.u), *dp = static_cast<const T *>(a.delta);
+    const T *zp = static_cast<const T *>(a.z);
+    const T *Bp = static_cast<const T *>(a.B), *Cp = static_cast<const T *>(a.C);
+
+    auto issue = [&](int j) {  // j-th tile of this CTA into stage j % kStreamStages
+        const int tile = blockIdx.x + j * gridDim.x;
+        const size_t ch0 = (size_t)tile * kStreamCh;
+        const size_t bb = tile / tiles_per_seq;
+        const int d0 = (tile % tiles_per_seq) * kStreamCh;
+        unsigned char *st = smem + (j % kStreamStages) * S::bytes;
+        uint64_t *b = &bar[j % kStreamStages];
+        (void)d0;
+        uint32_t bytes = kStreamCh * 64 + 2 * kStreamCh * S::ES + 2 * 16 * S::ES;
+        if (HAS_Z) bytes += kStreamCh * S::ES;
+        mbar_arrive_expect_tx(b, bytes);
+        bulk_load(st + S::off_h, a.state + ch0 * 16, kStreamCh * 64, b);
+        bulk_load(st + S::off_u, up + ch0, kStreamCh * S::ES, b);
+        bulk_load(st + S::off_d, dp + ch0, kStreamCh * S::ES, b);
+        if (HAS_Z) bulk_load(st + S::off_z, zp + ch0, kStreamCh * S::ES, b);
+        bulk_load(st + S::off_B, Bp + bb * 16, 16 * S::ES, b);
+        bulk_load(st + S::off_C, Cp + bb * 16, 16 * S::ES, b);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStreamStages; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+        for (int j = 0; j < kStreamAhead && j < nmine; ++j) issue(j);
+    }
+    __syncthreads();
+
+    // Per-thread rows that do not depend on the sequence: A words, bias, D,
+    // loaded one tile ahead into registers.
+    const int g = tid & 3;
+    float4 an[4];
+    float bn[4], kn[4];
+    auto prefetch = [&](int j) {
+        const int tile = blockIdx.x + j * gridDim.x;
+        const int d0 = (tile % tiles_per_seq) * kStreamCh;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = (i * kStreamCh + tid) >> 2;
+            an[i] = __ldg(reinterpret_cast<const float4 *>(a.A + (size_t)(d0 + c) * 16) + g);
+            bn[i] = a.bias ? __ldg(a.bias + d0 + c) : 0.f;
+            kn[i] = a.Dskip ? __ldg(a.Dskip + d0 + c) : 0.f;
+        }
+    };
+    if (nmine > 0) prefetch(0);
+
+    bool failed = false;
+    for (int j = 0; j < nmine; ++j) {
+        const int s = j % kStreamStages;
+        unsigned char *st = smem + s * S::bytes;
+        // Load tile j + ahead into the stage of tile j + ahead - stages (= j - 2),
+        // whose store (the older of the two pending) must have read it first.
+        if (tid == 0 && j + kStreamAhead < nmine) {
+            bulk_wait_read1();
+            issue(j + kStreamAhead);
+        }
+        float4 ac[4];
+        float bc[4], kc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ac[i] = an[i];
+            bc[i] = bn[i];
+            kc[i] = kn[i];
+        }
+        if (j + 1 < nmine) prefetch(j + 1);
+        const bool ok = mbar_wait_bounded(&bar[s], (j / kStreamStages) & 1, 1u << 22);
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        const int tile = blockIdx.x + j * gridDim.x;
+        float4 *hs = reinterpret_cast<float4 *>(st + S::off_h);
+        const T *us = reinterpret_cast<const T *>(st + S::off_u);
+        const T *ds = reinterpret_cast<const T *>(st + S::off_d);
+        const T *zs = reinterpret_cast<const T *>(st + S::off_z);
+        const T *Bs = reinterpret_cast<const T *>(st + S::off_B);
+        const T *Cs = reinterpret_cast<const T *>(st + S::off_C);
+        T *ys = reinterpret_cast<T *>(st + S::off_y);
+        float bv[4], cv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            bv[k] = IO<T>::to_f(Bs[4 * g + k]);
+            cv[k] = IO<T>::to_f(Cs[4 * g + k]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int w = i * kStreamCh + tid;  // state word: channel w / 4, states 4g .. 4g+3
+            const int c = w >> 2;
+            const float4 hv = hs[w];
+            const float4 av = ac[i];
+            const float u = IO<T>::to_f(us[c]);
+            float dl = IO<T>::to_f(ds[c]) + bc[i];
+            if (a.delta_softplus) dl = softplus(dl);
+            const float du = dl * u;
+            const float avv[4] = {av.x, av.y, av.z, av.w};
+            float h4[4] = {hv.x, hv.y, hv.z, hv.w};
+            float part = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float abar = ex2(dl * (avv[k] * kLog2e));
+                h4[k] = fmaf(abar, h4[k], bv[k] * du);
+                part = fmaf(cv[k], h4[k], part);
+            }
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            hs[w] = make_float4(h4[0], h4[1], h4[2], h4[3]);
+            if (g == 0) {
+                float out = part + kc[i] * u;
+                if (HAS_Z) out *= gate_of<T>(IO<T>::to_f(zs[c]));
+                ys[c] = IO<T>::from_f(out);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            const size_t ch0 = (size_t)tile * kStreamCh;
+            bulk_store(a.state + ch0 * 16, st + S::off_h, kStreamCh * 64);
+            bulk_store(static_cast<T *>(a.y) + ch0, st + S::off_y, kStreamCh * S::ES);
+            bulk_commit();
+        }
+    }
+    // A wait that ran out (never expected) leaves the remaining tiles of this
+    // CTA unprocessed; the copies already issued are drained first.
+    if (tid == 0) {
+        bulk_wait0();
+        if (failed)
+            for (int s = 0; s < kStreamStages; ++s) (void)mbar_wait_bounded(&bar[s], 0, 1u << 20);
+    }
+}
+
 namespace {
+template <typename T>
+cudaError_t stream_dispatch(const StepArgs &a, cudaStream_t st) {
+    using S = StreamTile<T>;
+    const int smem = kStreamStages * S::bytes + 64;
+    const int ntiles = (int)((size_t)a.batch * a.dim / kStreamCh);
+    static int grid_cap = 0;
+    if (grid_cap == 0) {
+        auto k0 = step_stream_kernel<T, false>;
+        auto k1 = step_stream_kernel<T, true>;
+        if (cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return cudaGetLastError();
+        int per_sm = 0, dev = 0, sms = 148;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k1, kStreamCh, smem) != cudaSuccess) return cudaGetLastError();
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        grid_cap = sms * (per_sm > 0 ? per_sm : 1);
+    }
+    const int grid = ntiles < grid_cap ? ntiles : grid_cap;
+    if (a.z) step_stream_kernel<T, true><<<grid, kStreamCh, smem, st>>>(a);
+    else step_stream_kernel<T, false><<<grid, kStreamCh, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t wide_dispatch(const StepArgs &a, cudaStream_t st) {
     const size_t words = (size_t)a.batch * a.dim * 4;
@@ -203,6 +396,15 @@ cudaError_t step_launch(const StepArgs &a, bool bf16, cudaStream_t st) {
     // The wide kernel reads rows of 16 states as 16-byte words: N = 16 and
     // 16-byte aligned state, A, B and C (a 16-state row is 32 or 64 bytes).
     const bool wide = a.dstate == 16 && aligned16(a.state) && aligned16(a.A) && aligned16(a.B) && aligned16(a.C);
+    // The bulk-copy stream also needs whole 128-channel tiles within one
+    // sequence and 16-byte aligned per-channel arrays.
+#ifndef SSM_STEP_STREAM
+#define SSM_STEP_STREAM 1
+#endif
+    const bool stream = SSM_STEP_STREAM && wide && a.dim % kStreamCh == 0 && aligned16(a.u) && aligned16(a.delta) &&
+                        (!a.z || aligned16(a.z)) && (!a.bias || aligned16(a.bias)) && (!a.Dskip || aligned16(a.Dskip)) &&
+                        aligned16(a.y);
+    if (stream) return bf16 ? stream_dispatch<__nv_bfloat16>(a, st) : stream_dispatch<float>(a, st);
     if (wide) return bf16 ? wide_dispatch<__nv_bfloat16>(a, st) : wide_dispatch<float>(a, st);
     return bf16 ? step_ng<__nv_bfloat16>(a, st) : step_ng<float>(a, st);
 }
