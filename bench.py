@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-other", action="store_true", help="skip the other scan workloads")
     ap.add_argument("--settle-s", type=float, default=0.5,
                     help="seconds of untimed load before the timed region (clock settling)")
     return ap.parse_args()
@@ -53,6 +54,37 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "MEASURED_PEAKS.json (copy, measured)"
     return HBM_FALLBACK_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ ncu record
+TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {
+    "scan_kernel": ["scan_fwd.cu", "ssm_device.cuh", "ssm_internal.h"],
+    "step_stream_kernel": ["state_update.cu", "ssm_device.cuh", "ssm_internal.h"],
+}
+
+
+def source_hash(kernel: str) -> str:
+    """sha256 over the CUDA sources a kernel is built from."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "mamba_selective_scan_02_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu record, or None when the
+    record is missing or was taken on different kernel sources."""
+    try:
+        with open(TRAFFIC) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 # ------------------------------------------------------------------ clocks
@@ -243,7 +275,17 @@ def run_ours(args):
                         inp["bias"], None, y=y, hL=hL, workspace=ws)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    launches_per_step = 1 if ws.numel() <= 256 else 3   # one chunk: a single kernel
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        """Evict L2: write a buffer twice its size, then read another one, so the
+        dirty lines are written back before (not during) the timed launch."""
+        flush_w.zero_()
+        flush_r.sum()
+    plan = capi.ssm_scan_plan(p)
+    # one scan kernel, or aggregate + carry + scan kernels in two-pass mode
+    launches_per_step = 1 if (plan["chained"] or plan["nchunks"] == 1) else 3
 
     # MUFU ex2 peak, measured on this GPU (the roofline's exponential side)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -305,11 +347,12 @@ def run_ours(args):
         "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
                    "seqlen": w.seqlen, "io_dtype": w.io_dtype, "state_dtype": "f32",
                    "parallelism": f"replicas x{world} (independent channels)",
+                   "scan_plan": plan,
                    "l2": f"inputs larger than L2 ({alg_bytes / 1e6:.1f} MB per step)"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {
             "bound": "alu", "unit": "Gex2/s", "achieved": achieved_ex2, "peak": mufu_peak,
-            "frac": achieved_ex2 / mufu_peak, "traffic": None,
+            "frac": achieved_ex2 / mufu_peak, "traffic": recorded_traffic("scan_kernel"),
             "peak_source": "MUFU ex2.approx throughput measured in this run (ssm_bench_mufu_ex2)",
             "kernel_ms": kern_ms,
             "hbm": {"achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
@@ -319,6 +362,43 @@ def run_ours(args):
         },
         "clocks": clocks.summary(),
     }
+
+    # ---- the other scan workloads (parity cases), timed the same way, kernel only
+    if not args.no_other:
+        others = {}
+        for name in ("small_layer_L2048", "long_seq_L131072"):
+            wo = WORKLOADS[name]
+            oi = make_inputs(wo, device=dev)
+            oy = torch.empty_like(oi["u"])
+            oh = torch.empty((wo.batch, wo.dim, wo.dstate), dtype=torch.float32, device=dev)
+            ows = torch.empty(api.workspace_bytes(oi["u"], oi["delta"], oi["A"], oi["B"], oi["C"]),
+                              dtype=torch.uint8, device=dev)
+            op = api.scan_params(oi["u"], oi["delta"], oi["A"], oi["B"], oi["C"], oi["Dskip"], oi["z"],
+                                 oi["bias"], None, y=oy, hL=oh, workspace=ows)
+            reps = 3 if wo.seqlen > 100000 else 50
+            for _ in range(3):
+                capi.ssm_scan_fwd(op, sh)
+            tms = []
+            for _ in range(reps):
+                flush_l2()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                capi.ssm_scan_fwd(op, sh)
+                e1.record(stream)
+                tms.append((e0, e1))
+            torch.cuda.synchronize(dev)
+            capi.check(api.workspace_status(ows), name)
+            oms = statistics.median(a_.elapsed_time(b_) for a_, b_ in tms)
+            oel = wo.batch * wo.dim * wo.seqlen
+            oex = exps_scan(wo.batch, wo.dim, wo.dstate, wo.seqlen)
+            obytes = algorithmic_bytes_scan(wo.batch, wo.dim, wo.dstate, wo.seqlen, 2)
+            others[name] = {"ms": oms, "Gelem_s": oel / (oms / 1e3) / 1e9,
+                            "mufu_frac": oex / (oms / 1e3) / 1e9 / mufu_peak,
+                            "hbm_frac": obytes / (oms / 1e3) / 1e9 / hbm_peak,
+                            "l2": "L2 flushed before every timed launch (256 MB written, 256 MB read)"}
+            out["gpu_launches"] += reps + 3
+            del oi, oy, oh, ows
+        out["other_workloads"] = others
 
     # ---- end to end through the C ABI from pinned host buffers
     if not args.no_e2e:
@@ -365,7 +445,6 @@ def run_ours(args):
         dinp = make_inputs(wd, device=dev)
         state = dinp["h0"].clone()
         ydec = torch.empty((wd.batch, wd.dim), dtype=dinp["u"].dtype, device=dev)
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         tok = [api.step_params(state, dinp["u"][t], dinp["delta"][t], dinp["A"], dinp["B"][t], dinp["C"][t],
                                dinp["Dskip"], dinp["z"][t], dinp["bias"], y=ydec) for t in range(wd.seqlen)]
         for t in range(4):
@@ -374,7 +453,7 @@ def run_ours(args):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(wd.seqlen)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(wd.seqlen)]
         for t in range(wd.seqlen):
-            flush.zero_()
+            flush_l2()
             starts[t].record(stream)
             capi.ssm_state_update(tok[t], sh)
             ends[t].record(stream)
@@ -386,9 +465,11 @@ def run_ours(args):
         out["decode"] = {"workload": wd.name, "tokens": wd.seqlen, "ms_per_token": mean_ms,
                          "value": wd.batch * wd.dim / (mean_ms / 1e3) / 1e9, "unit": UNIT,
                          "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                                      "frac": gbs / hbm_peak, "traffic": None,
+                                      "frac": gbs / hbm_peak,
+                                      "traffic": recorded_traffic("step_stream_kernel"),
                                       "algorithmic_bytes": dbytes},
-                         "l2": "256 MB written before every token; state 83.9 MB"}
+                         "l2": "L2 flushed before every token (256 MB written, then another 256 MB read "
+                               "so the written lines are back in HBM); state 83.9 MB"}
         out["gpu_launches"] += wd.seqlen + 4
 
     # ---- CPU baseline: the fp64 oracle on a bounded sample (rank 0 only)

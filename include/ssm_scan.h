@@ -85,14 +85,23 @@ typedef struct {
     void *workspace;        /* device scratch of >= ssm_scan_workspace_size(...) bytes */
     size_t workspace_bytes;
     int64_t chunk_len;      /* 0 = automatic.  Otherwise the sequence is cut into
-                               chunks of this many tokens (a multiple of 64) that
-                               run in parallel and are joined by carried states. */
+                               chunks of this many tokens (a multiple of 64),
+                               joined by carried states (see ssm_scan_plan). */
 } ssm_scan_params;
 
 /* Bytes of workspace ssm_scan_fwd needs for these sizes and chunk_len (never 0:
  * the workspace always holds the device status word).  Returns 0 only when the
  * sizes are invalid. */
 size_t ssm_scan_workspace_size(const ssm_scan_params *p);
+
+/* How ssm_scan_fwd will cut this scan into work items (host-side, no GPU
+ * needed).  On SSM_OK fills out[0] = tokens per chunk, out[1] = number of
+ * chunks K, out[2] = 1 if chunk k starts from the state chunk k-1 hands over
+ * (one kernel launch) or 0 if an aggregate pass and a carry pass precompute the
+ * chunks' starting states (three launches when K > 1), out[3] = number of
+ * channel groups (one warp each).  Returns SSM_ERR_INVALID_ARG for invalid
+ * sizes or a NULL out. */
+ssm_status ssm_scan_plan(const ssm_scan_params *p, int64_t out[4]);
 
 /* Forward selective scan: writes y and (if non-NULL) hL.  Also clears the
  * workspace status word before launching. */

@@ -69,6 +69,8 @@ def lib():
             L = ctypes.CDLL(path)
             L.ssm_scan_workspace_size.restype = ctypes.c_size_t
             L.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanParams)]
+            L.ssm_scan_plan.restype = ctypes.c_int
+            L.ssm_scan_plan.argtypes = [ctypes.POINTER(ScanParams), ctypes.POINTER(_i64)]
             L.ssm_scan_fwd.restype = ctypes.c_int
             L.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanParams), _vp]
             L.ssm_scan_fwd_noalloc.restype = ctypes.c_int
@@ -104,6 +106,13 @@ def check(code: int, where: str) -> None:
 
 def ssm_scan_workspace_size(p: ScanParams) -> int:
     return lib().ssm_scan_workspace_size(ctypes.byref(p))
+
+
+def ssm_scan_plan(p: ScanParams) -> dict:
+    """The scan's work split: chunk_len, nchunks, chained, groups."""
+    out = (_i64 * 4)()
+    check(lib().ssm_scan_plan(ctypes.byref(p), out), "ssm_scan_plan")
+    return {"chunk_len": out[0], "nchunks": out[1], "chained": bool(out[2]), "groups": out[3]}
 
 
 def ssm_scan_fwd(p: ScanParams, stream: int) -> int:

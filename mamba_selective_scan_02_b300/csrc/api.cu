@@ -68,11 +68,21 @@ size_t ssm_scan_workspace_size(const ssm_scan_params *p) {
     return scan_layout(p).total;
 }
 
+ssm_status ssm_scan_plan(const ssm_scan_params *p, int64_t out[4]) {
+    if (!scan_sizes_ok(p) || !out) return SSM_ERR_INVALID_ARG;
+    const ssm::ScanPlan plan = scan_layout(p).plan;
+    out[0] = plan.chunk_len;
+    out[1] = plan.nchunks;
+    out[2] = plan.chained ? 1 : 0;
+    out[3] = plan.groups;
+    return SSM_OK;
+}
+
 ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream) {
     if (!scan_sizes_ok(p)) return SSM_ERR_INVALID_ARG;
     if (p->io_dtype != SSM_F32 && p->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
     if (p->dstate > SSM_MAX_DSTATE) return SSM_ERR_UNSUPPORTED;
-    if (p->zoh != 0) return SSM_ERR_UNSUPPORTED;
+    if (p->zoh != 0 && p->zoh != 1) return SSM_ERR_INVALID_ARG;
     if (p->delta_softplus != 0 && p->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
     if (!p->u || !p->delta || !p->B || !p->C || !p->A || !p->y || !p->workspace) return SSM_ERR_INVALID_ARG;
     const void *a16[] = {p->u, p->delta, p->z, p->B, p->C, p->y, p->h0, p->hL, p->workspace};
@@ -109,6 +119,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream) {
     a.Dskip = p->Dskip;
     a.bias = p->delta_bias;
     a.delta_softplus = p->delta_softplus;
+    a.zoh = p->zoh;
     a.h0 = p->h0;
     a.y = p->y;
     a.hL = p->hL;
@@ -130,7 +141,7 @@ ssm_status ssm_state_update(const ssm_step_params *p, ssm_stream_t stream) {
     if (p->batch * p->dim > (int64_t(1) << 31) / 4) return SSM_ERR_UNSUPPORTED;
     if (p->io_dtype != SSM_F32 && p->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
     if (p->dstate > SSM_MAX_DSTATE) return SSM_ERR_UNSUPPORTED;
-    if (p->zoh != 0) return SSM_ERR_UNSUPPORTED;
+    if (p->zoh != 0 && p->zoh != 1) return SSM_ERR_INVALID_ARG;
     if (p->delta_softplus != 0 && p->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
     if (!p->state || !p->u || !p->delta || !p->B || !p->C || !p->A || !p->y) return SSM_ERR_INVALID_ARG;
     // The decode kernel reads every input with scalar loads, so element
@@ -162,6 +173,7 @@ ssm_status ssm_state_update(const ssm_step_params *p, ssm_stream_t stream) {
     a.Dskip = p->Dskip;
     a.bias = p->delta_bias;
     a.delta_softplus = p->delta_softplus;
+    a.zoh = p->zoh;
     a.y = p->y;
     return ssm::step_launch(a, p->io_dtype == SSM_BF16, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? SSM_OK

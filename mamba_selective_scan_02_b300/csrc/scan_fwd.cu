@@ -124,7 +124,7 @@ struct Item {
 
 // MODE 0: scan writing y (and hL after the last chunk).
 // MODE 1: chunk aggregate (Π Ā, h_end from zero) for chunks 0..K-2 (two-pass).
-template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, int MODE>
+template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, int MODE, bool ZOH>
 __global__ void __launch_bounds__(32, 1)
 scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     using S = WTile<T, SPT, NG>;
@@ -390,6 +390,13 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                         ao[2 * q4 + 1] = make_float2(ex2(x1.x), ex2(x1.y));
                         bo[2 * q4] = __fmul2_rn(make_float2(bq.x, bq.y), du2);
                         bo[2 * q4 + 1] = __fmul2_rn(make_float2(bq.z, bq.w), du2);
+                        if (ZOH) {  // B̄ = Δ·φ(ΔA)·B; x0, x1 hold ΔA·log2e
+                            const float2 n0 = __fmul2_rn(x0, make_float2(kLn2, kLn2));
+                            const float2 n1 = __fmul2_rn(x1, make_float2(kLn2, kLn2));
+                            bo[2 * q4] = __fmul2_rn(bo[2 * q4], make_float2(zoh_phi(n0.x, ao[2 * q4].x), zoh_phi(n0.y, ao[2 * q4].y)));
+                            bo[2 * q4 + 1] = __fmul2_rn(bo[2 * q4 + 1], make_float2(zoh_phi(n1.x, ao[2 * q4 + 1].x),
+                                                                                   zoh_phi(n1.y, ao[2 * q4 + 1].y)));
+                        }
                     }
                 };
                 decay_input(0, an, bn);
@@ -594,10 +601,10 @@ Split split_for(int64_t dstate) {
     return SSM_SCAN_N16_LANES == 1 ? Split{16, 1} : Split{8, 2};
 }
 
-template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, int MODE>
+template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, int MODE, bool ZOH>
 cudaError_t launch_one(const Maps &maps, const ScanArgs &a, int items, cudaStream_t st) {
     using S = WTile<T, SPT, NG>;
-    auto kern = scan_kernel<T, SPT, NG, HAS_Z, TMA, MODE>;
+    auto kern = scan_kernel<T, SPT, NG, HAS_Z, TMA, MODE, ZOH>;
     static int per_sm = 0;  // resident warps per SM for this instantiation
     if (per_sm == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::bytes);
@@ -615,26 +622,33 @@ cudaError_t launch_one(const Maps &maps, const ScanArgs &a, int items, cudaStrea
     return cudaGetLastError();
 }
 
-template <typename T, int SPT, int NG, bool HAS_Z, bool TMA>
+template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, bool ZOH>
 cudaError_t launch_all(const Maps &maps, const ScanArgs &a, cudaStream_t st) {
     cudaError_t e;
     if (a.nchunks > 1 && !a.chained) {
-        e = launch_one<T, SPT, NG, false, TMA, 1>(maps, a, a.groups * (a.nchunks - 1), st);
+        e = launch_one<T, SPT, NG, false, TMA, 1, ZOH>(maps, a, a.groups * (a.nchunks - 1), st);
         if (e != cudaSuccess) return e;
         const size_t total = (size_t)a.batch * a.dim * a.dstate;
         carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    return launch_one<T, SPT, NG, HAS_Z, TMA, 0>(maps, a, a.groups * a.nchunks, st);
+    return launch_one<T, SPT, NG, HAS_Z, TMA, 0, ZOH>(maps, a, a.groups * a.nchunks, st);
 }
 
-template <typename T, int SPT, int NG>
-cudaError_t dispatch_z_tma(const Maps &maps, const ScanArgs &a, bool tma, cudaStream_t st) {
+template <typename T, int SPT, int NG, bool ZOH>
+cudaError_t dispatch_z_tma_d(const Maps &maps, const ScanArgs &a, bool tma, cudaStream_t st) {
     const bool z = a.z != nullptr;
     if (tma)
-        return z ? launch_all<T, SPT, NG, true, true>(maps, a, st) : launch_all<T, SPT, NG, false, true>(maps, a, st);
-    return z ? launch_all<T, SPT, NG, true, false>(maps, a, st) : launch_all<T, SPT, NG, false, false>(maps, a, st);
+        return z ? launch_all<T, SPT, NG, true, true, ZOH>(maps, a, st)
+                 : launch_all<T, SPT, NG, false, true, ZOH>(maps, a, st);
+    return z ? launch_all<T, SPT, NG, true, false, ZOH>(maps, a, st)
+             : launch_all<T, SPT, NG, false, false, ZOH>(maps, a, st);
+}
+template <typename T, int SPT, int NG>
+cudaError_t dispatch_z_tma(const Maps &maps, const ScanArgs &a, bool tma, cudaStream_t st) {
+    return a.zoh ? dispatch_z_tma_d<T, SPT, NG, true>(maps, a, tma, st)
+                 : dispatch_z_tma_d<T, SPT, NG, false>(maps, a, tma, st);
 }
 
 template <typename T>

@@ -77,6 +77,19 @@ __device__ __forceinline__ float softplus_mufu(float x) {
     return fmaf(lg2(1.0f + w), kLn2, fmaxf(x, 0.0f));
 }
 
+// Exact zero-order hold: B̄ = (e^{ΔA} − 1)/A · B = Δ·φ(x)·B with x = Δ·A and
+// φ(x) = (e^x − 1)/x ("Discretisation: zero-order hold", first-principles page).
+// φ is a Taylor polynomial for |x| < 1/8 (next term x^6/5040 < 8e-11), where
+// e^x − 1 would cancel, and (Ā − 1)/x above; `abar` is e^x already computed.
+__device__ __forceinline__ float zoh_phi(float x, float abar) {
+    float p = fmaf(x, 1.0f / 720.0f, 1.0f / 120.0f);
+    p = fmaf(x, p, 1.0f / 24.0f);
+    p = fmaf(x, p, 1.0f / 6.0f);
+    p = fmaf(x, p, 0.5f);
+    p = fmaf(x, p, 1.0f);
+    return fabsf(x) < 0.125f ? p : __fdividef(abar - 1.0f, x);
+}
+
 // silu(z) = z·σ(z).  Accurate form (fp32 I/O): z / (1 + 2^{-z·log2e}).
 __device__ __forceinline__ float silu_accurate(float z) {
     return z * rcp_approx(1.0f + ex2(-z * kLog2e));

@@ -12,6 +12,7 @@ struct ScanArgs {
     const void *u, *delta, *z, *B, *C;
     const float *A, *Dskip, *bias;
     int delta_softplus;
+    int zoh;         // 1: exact zero-order-hold B̄
     const float *h0;
     void *y;
     float *hL;
@@ -45,6 +46,7 @@ struct StepArgs {
     const void *u, *delta, *z, *B, *C;
     const float *A, *Dskip, *bias;
     int delta_softplus;
+    int zoh;
     void *y;
 };
 

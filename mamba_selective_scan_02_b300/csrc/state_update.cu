@@ -21,7 +21,7 @@
 
 namespace ssm {
 
-template <typename T, int NG, bool VEC, bool HAS_Z>
+template <typename T, int NG, bool VEC, bool HAS_Z, bool ZOH>
 __global__ void __launch_bounds__(256) step_kernel(const StepArgs a) {
     const size_t gid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const size_t items = (size_t)a.batch * a.dim * NG;
@@ -61,8 +61,10 @@ __global__ void __launch_bounds__(256) step_kernel(const StepArgs a) {
     for (int j = 0; j < 4; ++j) {
         const int n = 4 * g + j;
         if (live && n < N) {
-            const float abar = ex2(dv * (a.A[(size_t)d * N + n] * kLog2e));
-            hv[j] = fmaf(abar, hv[j], IO<T>::to_f(B[bb * N + n]) * du);
+            const float an = a.A[(size_t)d * N + n];
+            const float abar = ex2(dv * (an * kLog2e));
+            const float bbar = ZOH ? zoh_phi(dv * an, abar) : 1.f;  // exact ZOH: B̄ = Δ·φ(ΔA)·B
+            hv[j] = fmaf(abar, hv[j], IO<T>::to_f(B[bb * N + n]) * du * bbar);
             part = fmaf(IO<T>::to_f(C[bb * N + n]), hv[j], part);
         }
     }
@@ -95,7 +97,7 @@ constexpr int kStepThreads = 128;
 #endif
 constexpr int kStepIPT = SSM_STEP_IPT;
 
-template <typename T, bool HAS_Z>
+template <typename T, bool HAS_Z, bool ZOH>
 __global__ void __launch_bounds__(kStepThreads) step_wide_kernel(const StepArgs a) {
     const size_t words = (size_t)a.batch * a.dim * 4;  // 16-byte state words
     const size_t base = (size_t)blockIdx.x * (kStepThreads * kStepIPT) + threadIdx.x;
@@ -150,7 +152,8 @@ __global__ void __launch_bounds__(kStepThreads) step_wide_kernel(const StepArgs 
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float abar = ex2(delta * (avv[j] * kLog2e));
-            h4[j] = fmaf(abar, h4[j], bv[i][j] * du);
+            const float bbar = ZOH ? zoh_phi(delta * avv[j], abar) : 1.f;
+            h4[j] = fmaf(abar, h4[j], bv[i][j] * du * bbar);
             part = fmaf(cv[i][j], h4[j], part);
         }
         part += __shfl_xor_sync(0xffffffffu, part, 1);
@@ -194,7 +197,7 @@ template <typename T> struct StreamTile {
     static constexpr int bytes = (off_y + kStreamCh * ES + 127) / 128 * 128;
 };
 
-template <typename T, bool HAS_Z>
+template <typename T, bool HAS_Z, bool ZOH>
 __global__ void __launch_bounds__(kStreamCh) step_stream_kernel(const StepArgs a) {
     using S = StreamTile<T>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -305,7 +308,8 @@ __global__ void __launch_bounds__(kStreamCh) step_stream_kernel(const StepArgs a
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float abar = ex2(dl * (avv[k] * kLog2e));
-                h4[k] = fmaf(abar, h4[k], bv[k] * du);
+                const float bbar = ZOH ? zoh_phi(dl * avv[k], abar) : 1.f;
+                h4[k] = fmaf(abar, h4[k], bv[k] * du * bbar);
                 part = fmaf(cv[k], h4[k], part);
             }
             part += __shfl_xor_sync(0xffffffffu, part, 1);
@@ -343,10 +347,14 @@ cudaError_t stream_dispatch(const StepArgs &a, cudaStream_t st) {
     const int ntiles = (int)((size_t)a.batch * a.dim / kStreamCh);
     static int grid_cap = 0;
     if (grid_cap == 0) {
-        auto k0 = step_stream_kernel<T, false>;
-        auto k1 = step_stream_kernel<T, true>;
+        auto k0 = step_stream_kernel<T, false, false>;
+        auto k1 = step_stream_kernel<T, true, false>;
+        auto k2 = step_stream_kernel<T, false, true>;
+        auto k3 = step_stream_kernel<T, true, true>;
         if (cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-            cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return cudaGetLastError();
         int per_sm = 0, dev = 0, sms = 148;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k1, kStreamCh, smem) != cudaSuccess) return cudaGetLastError();
@@ -354,8 +362,13 @@ cudaError_t stream_dispatch(const StepArgs &a, cudaStream_t st) {
         grid_cap = sms * (per_sm > 0 ? per_sm : 1);
     }
     const int grid = ntiles < grid_cap ? ntiles : grid_cap;
-    if (a.z) step_stream_kernel<T, true><<<grid, kStreamCh, smem, st>>>(a);
-    else step_stream_kernel<T, false><<<grid, kStreamCh, smem, st>>>(a);
+    if (a.zoh) {
+        if (a.z) step_stream_kernel<T, true, true><<<grid, kStreamCh, smem, st>>>(a);
+        else step_stream_kernel<T, false, true><<<grid, kStreamCh, smem, st>>>(a);
+    } else {
+        if (a.z) step_stream_kernel<T, true, false><<<grid, kStreamCh, smem, st>>>(a);
+        else step_stream_kernel<T, false, false><<<grid, kStreamCh, smem, st>>>(a);
+    }
     return cudaGetLastError();
 }
 
@@ -363,22 +376,31 @@ template <typename T>
 cudaError_t wide_dispatch(const StepArgs &a, cudaStream_t st) {
     const size_t words = (size_t)a.batch * a.dim * 4;
     const unsigned blocks = (unsigned)((words + kStepThreads * kStepIPT - 1) / (kStepThreads * kStepIPT));
-    if (a.z) step_wide_kernel<T, true><<<blocks, kStepThreads, 0, st>>>(a);
-    else step_wide_kernel<T, false><<<blocks, kStepThreads, 0, st>>>(a);
+    if (a.zoh) {
+        if (a.z) step_wide_kernel<T, true, true><<<blocks, kStepThreads, 0, st>>>(a);
+        else step_wide_kernel<T, false, true><<<blocks, kStepThreads, 0, st>>>(a);
+    } else {
+        if (a.z) step_wide_kernel<T, true, false><<<blocks, kStepThreads, 0, st>>>(a);
+        else step_wide_kernel<T, false, false><<<blocks, kStepThreads, 0, st>>>(a);
+    }
     return cudaGetLastError();
 }
 
-template <typename T, int NG>
-cudaError_t step_dispatch(const StepArgs &a, cudaStream_t st) {
+template <typename T, int NG, bool ZOH>
+cudaError_t step_dispatch_z(const StepArgs &a, cudaStream_t st) {
     const size_t items = (size_t)a.batch * a.dim * NG;
     const unsigned blocks = (unsigned)((items + 255) / 256);
     const bool vec = a.dstate % 4 == 0 && (reinterpret_cast<uintptr_t>(a.state) & 15) == 0;
     const bool z = a.z != nullptr;
-    if (vec && z) step_kernel<T, NG, true, true><<<blocks, 256, 0, st>>>(a);
-    else if (vec) step_kernel<T, NG, true, false><<<blocks, 256, 0, st>>>(a);
-    else if (z) step_kernel<T, NG, false, true><<<blocks, 256, 0, st>>>(a);
-    else step_kernel<T, NG, false, false><<<blocks, 256, 0, st>>>(a);
+    if (vec && z) step_kernel<T, NG, true, true, ZOH><<<blocks, 256, 0, st>>>(a);
+    else if (vec) step_kernel<T, NG, true, false, ZOH><<<blocks, 256, 0, st>>>(a);
+    else if (z) step_kernel<T, NG, false, true, ZOH><<<blocks, 256, 0, st>>>(a);
+    else step_kernel<T, NG, false, false, ZOH><<<blocks, 256, 0, st>>>(a);
     return cudaGetLastError();
+}
+template <typename T, int NG>
+cudaError_t step_dispatch(const StepArgs &a, cudaStream_t st) {
+    return a.zoh ? step_dispatch_z<T, NG, true>(a, st) : step_dispatch_z<T, NG, false>(a, st);
 }
 template <typename T>
 cudaError_t step_ng(const StepArgs &a, cudaStream_t st) {

@@ -79,7 +79,7 @@ def valid_scan(**over):
     (dict(chunk_len=100), capi.SSM_ERR_INVALID_ARG),        # not a multiple of 64
     (dict(chunk_len=-64), capi.SSM_ERR_INVALID_ARG),
     (dict(delta_softplus=2), capi.SSM_ERR_INVALID_ARG),
-    (dict(zoh=1), capi.SSM_ERR_UNSUPPORTED),
+    (dict(zoh=2), capi.SSM_ERR_INVALID_ARG),
 ])
 def test_scan_rejects_before_launch(over, code):
     assert capi.ssm_scan_fwd(valid_scan(**over), None) == code
@@ -115,6 +115,16 @@ def test_workspace_size():
     assert capi.ssm_scan_fwd(p, None) == capi.SSM_ERR_INVALID_ARG
 
 
+def test_scan_plan():
+    plan = capi.ssm_scan_plan(valid_scan(batch=4, dim=5120, seqlen=2048))
+    assert plan == {"chunk_len": 256, "nchunks": 8, "chained": True, "groups": 1280}
+    plan = capi.ssm_scan_plan(valid_scan(batch=1, dim=5120, seqlen=131072))
+    assert not plan["chained"] and plan["nchunks"] > 1 and plan["chunk_len"] % 64 == 0
+    plan = capi.ssm_scan_plan(valid_scan(batch=1, dim=64, seqlen=256))
+    assert plan["nchunks"] == 1 and not plan["chained"]
+    assert capi.lib().ssm_scan_plan(None, None) == capi.SSM_ERR_INVALID_ARG
+
+
 def valid_step(**over):
     p = capi.StepParams()
     p.batch, p.dim, p.dstate = 4, 64, 16
@@ -137,7 +147,7 @@ def valid_step(**over):
     (dict(u=FAKE + (1 << 20) + 1), capi.SSM_ERR_INVALID_ARG),  # bf16 input at an odd address
     (dict(y=FAKE + 1 * (1 << 20)), capi.SSM_ERR_INVALID_ARG),  # y is u
     (dict(io_dtype=3), capi.SSM_ERR_INVALID_ARG),
-    (dict(zoh=1), capi.SSM_ERR_UNSUPPORTED),
+    (dict(zoh=2), capi.SSM_ERR_INVALID_ARG),
 ])
 def test_step_rejects_before_launch(over, code):
     assert capi.ssm_state_update(valid_step(**over), None) == code

@@ -59,6 +59,16 @@ def test_small_shapes(b, D, N, L, dtype, opts):
     _check(inp, dtype, f"{b}x{D}x{N}x{L} {dtype}", chunk_len=chunk, delta_softplus=softplus)
 
 
+def test_chained_chunks_every_element():
+    """Enough channel groups that chunk k starts from the state chunk k-1 hands
+    over (one warp per 16 channels; 3,600 channels leave a partial group)."""
+    inp = _case(4, 3600, 16, 512, torch.bfloat16, seed=21, h0=True)
+    p = capi.ScanParams()
+    p.batch, p.dim, p.dstate, p.seqlen, p.chunk_len = 4, 3600, 16, 512, 64
+    assert capi.ssm_scan_plan(p)["chained"]
+    _check(inp, torch.bfloat16, "chained 4x3600x16x512", chunk_len=64)
+
+
 def test_small_layer_workload_full():
     """The 2 × 1536 × 16 × 2048 bf16 layer, every channel checked."""
     _check(make_inputs("small_layer_L2048"), torch.bfloat16, "small_layer_L2048")
