@@ -79,7 +79,8 @@ template <typename T, int SPT, int NG> struct WTile {
     static constexpr int off_out = 2 * BUF;                      // two y tiles
     static constexpr int off_Bf = off_out + 2 * OUT;
     static constexpr int off_Cf = off_Bf + al128(kTT * BCP * 4);
-    static constexpr int off_bar = off_Cf + al128(kTT * BCP * 4);
+    static constexpr int off_ex = off_Cf + al128(kTT * BCP * 4);  // (Δ, Δ·u) of one 8-token block
+    static constexpr int off_bar = off_ex + al128(CPW * 5 * 16);  // 5 slots per channel: 4 + 1 pad
     static constexpr int bytes = off_bar + 16;
 };
 
@@ -94,6 +95,9 @@ template <> struct Pack<float> {
         reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
     __device__ __forceinline__ static void store2(float *p, float2 v) { *reinterpret_cast<float2 *>(p) = v; }
+    __device__ __forceinline__ static void store4(float *p, float2 a, float2 b) {
+        *reinterpret_cast<float4 *>(p) = make_float4(a.x, a.y, b.x, b.y);
+    }
 };
 template <> struct Pack<__nv_bfloat16> {
     __device__ __forceinline__ static uint32_t pk(float a, float b) {
@@ -105,6 +109,9 @@ template <> struct Pack<__nv_bfloat16> {
     }
     __device__ __forceinline__ static void store2(__nv_bfloat16 *p, float2 v) {
         *reinterpret_cast<uint32_t *>(p) = pk(v.x, v.y);
+    }
+    __device__ __forceinline__ static void store4(__nv_bfloat16 *p, float2 a, float2 b) {
+        *reinterpret_cast<uint2 *>(p) = make_uint2(pk(a.x, a.y), pk(b.x, b.y));
     }
 };
 
@@ -333,44 +340,69 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             const T *z_t = reinterpret_cast<const T *>(st + S::off_z);
 #pragma unroll 1
             for (int blk = 0; blk < NB8; ++blk) {
-                // ---- per-token terms of the channel's 8 tokens (both lanes of a
-                // channel form Δ and Δ·u; the gate only for the tokens they output)
+                // ---- per-token terms of the channel's 8 tokens.  With two lanes
+                // per channel, lane g forms Δ, Δ·u, the gate and D·u·gate of tokens
+                // 4g .. 4g+3 and the lanes swap Δ, Δ·u through shared memory.
                 const int eo = blk * (CPW * 8) + c * 8;
-                float uf[8], df[8], zf[8];
-                IO<T>::load8(u_t + eo, uf);
-                IO<T>::load8(d_t + eo, df);
-                if (MODE == 0 && HAS_Z) IO<T>::load8(z_t + eo, zf);
-                const int valid = it.t_end - (t0 + 8 * blk);  // tokens of this block inside the chunk
-                float2 dl[4], du[4];
+                constexpr int OWN = 8 / NG;        // tokens whose terms this lane forms
+                const int e0 = eo + OWN * g;      // its first token in the staged tile
+                const int valid = it.t_end - (t0 + 8 * blk) - OWN * g;  // of its tokens, inside the chunk
+                float uf[OWN], df[OWN], zf[OWN];
+                if (NG == 1) {
+                    IO<T>::load8(u_t + e0, uf);
+                    IO<T>::load8(d_t + e0, df);
+                    if (MODE == 0 && HAS_Z) IO<T>::load8(z_t + e0, zf);
+                } else {
+                    const float4 u4 = IO<T>::load4(u_t + e0), d4 = IO<T>::load4(d_t + e0);
+                    uf[0] = u4.x; uf[1] = u4.y; uf[2 % OWN] = u4.z; uf[3 % OWN] = u4.w;
+                    df[0] = d4.x; df[1] = d4.y; df[2 % OWN] = d4.z; df[3 % OWN] = d4.w;
+                    if (MODE == 0 && HAS_Z) {
+                        const float4 z4 = IO<T>::load4(z_t + e0);
+                        zf[0] = z4.x; zf[1] = z4.y; zf[2 % OWN] = z4.z; zf[3 % OWN] = z4.w;
+                    }
+                }
+                constexpr int OP = OWN / 2;        // own token pairs
+                float2 odl[OP], odu[OP];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < OP; ++j) {
                     float2 x = __fadd2_rn(make_float2(df[2 * j], df[2 * j + 1]), make_float2(bias, bias));
                     if (a.delta_softplus) x = make_float2(IO<T>::softplus(x.x), IO<T>::softplus(x.y));
-                    if (valid < 8) {  // Δ = 0 keeps the state: Ā = 1, B̄u = 0
+                    if (valid < OWN) {  // Δ = 0 keeps the state: Ā = 1, B̄u = 0
                         if (2 * j >= valid) x.x = 0.f;
                         if (2 * j + 1 >= valid) x.y = 0.f;
                     }
-                    dl[j] = x;
-                    du[j] = __fmul2_rn(x, make_float2(uf[2 * j], uf[2 * j + 1]));
+                    odl[j] = x;
+                    odu[j] = __fmul2_rn(x, make_float2(uf[2 * j], uf[2 * j + 1]));
                 }
-                // Gate and D·u·gate for the token pairs this lane outputs:
-                // NG = 1: all four pairs; NG = 2: pairs 2m + g of each half.
-                constexpr int OP = NG == 1 ? 4 : 2;
+                // Gate and D·u·gate of the lane's own tokens (the ones it outputs).
                 float2 gt[OP], dug[OP];
                 if (MODE == 0) {
 #pragma unroll
                     for (int m = 0; m < OP; ++m) {
-                        const int j0 = NG == 1 ? 2 * m : 4 * m;  // first token of the pair when g = 0
-                        float2 zz = make_float2(1.f, 1.f), uu;
-                        if (NG == 1) {
-                            uu = make_float2(uf[j0], uf[j0 + 1]);
-                            if (HAS_Z) zz = make_float2(zf[j0], zf[j0 + 1]);
-                        } else {
-                            uu = g ? make_float2(uf[j0 + 2], uf[j0 + 3]) : make_float2(uf[j0], uf[j0 + 1]);
-                            if (HAS_Z) zz = g ? make_float2(zf[j0 + 2], zf[j0 + 3]) : make_float2(zf[j0], zf[j0 + 1]);
-                        }
-                        gt[m] = HAS_Z ? gate2<T>(zz) : make_float2(1.f, 1.f);
+                        const float2 uu = make_float2(uf[2 * m], uf[2 * m + 1]);
+                        gt[m] = HAS_Z ? gate2<T>(make_float2(zf[2 * m], zf[2 * m + 1])) : make_float2(1.f, 1.f);
                         dug[m] = __fmul2_rn(__fmul2_rn(make_float2(skip, skip), uu), gt[m]);
+                    }
+                }
+                float2 dl[4], du[4];  // (Δ, Δ·u) of tokens (2j, 2j+1), as pairs over tokens
+                if (NG == 1) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        dl[j] = odl[j];
+                        du[j] = odu[j];
+                    }
+                } else {
+                    // [c][token pair] (Δ0, Δ1, Δu0, Δu1), rows padded to 5 slots against bank conflicts
+                    float4 *ex = reinterpret_cast<float4 *>(smem + S::off_ex) + c * 5;
+#pragma unroll
+                    for (int j = 0; j < OP; ++j)
+                        ex[OP * g + j] = make_float4(odl[j].x, odl[j].y, odu[j].x, odu[j].y);
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 v = ex[j];
+                        dl[j] = make_float2(v.x, v.y);
+                        du[j] = make_float2(v.z, v.w);
                     }
                 }
                 // ---- the recurrence over the block's 8 tokens.  Ā and B̄u of
@@ -452,18 +484,20 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                         }
                         Pack<T>::store8(out + eo, y);
                     } else {
-                        // Transposed sum over the two lanes of a channel, four
-                        // tokens at a time: lane g keeps tokens 4m + 2g, 4m + 2g + 1.
+                        // Transposed sum over the two lanes of a channel: lane g
+                        // keeps tokens 4g .. 4g+3, the ones whose gate it formed.
+                        float y[4];
 #pragma unroll
-                        for (int m = 0; m < 2; ++m) {
-                            const float k0 = g ? p[4 * m + 2] : p[4 * m], k1 = g ? p[4 * m + 3] : p[4 * m + 1];
-                            const float s0 = g ? p[4 * m] : p[4 * m + 2], s1 = g ? p[4 * m + 1] : p[4 * m + 3];
-                            const float r0 = __shfl_xor_sync(FULL, s0, 1), r1 = __shfl_xor_sync(FULL, s1, 1);
-                            const float2 y2 = __ffma2_rn(__fadd2_rn(make_float2(k0, k1), make_float2(r0, r1)), gt[m], dug[m]);
-                            Pack<T>::store2(out + eo + 4 * m + 2 * g, y2);
+                        for (int i = 0; i < 4; ++i) {
+                            const float keep = g ? p[4 + i] : p[i], send = g ? p[i] : p[4 + i];
+                            y[i] = keep + __shfl_xor_sync(FULL, send, 1);
                         }
+                        const float2 y01 = __ffma2_rn(make_float2(y[0], y[1]), gt[0], dug[0]);
+                        const float2 y23 = __ffma2_rn(make_float2(y[2], y[3]), gt[OP - 1], dug[OP - 1]);
+                        Pack<T>::store4(out + eo + 4 * g, y01, y23);
                     }
                 }
+                __syncwarp();  // the exchange buffer is rewritten by the next block
             }
 
             if (MODE == 0) {
