@@ -56,6 +56,34 @@ def measured_peaks():
     return HBM_FALLBACK_GBS, "fallback"
 
 
+# ------------------------------------------------------------------ ranks
+# Every rank scans its own copy of the workload: channels (and sequences) are
+# independent recurrences, so there is no data-path exchange between ranks.
+# Ranks meet only at the barriers around the timed region and in the max of
+# their timings.
+
+def rank_barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value of x over all ranks (the slowest rank's time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(elems_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job Gelem/s: the elements every rank processed over the slowest rank's time."""
+    return elems_per_rank * world / (ms_max / 1e3) / 1e9
+
+
 # ------------------------------------------------------------------ ncu record
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
@@ -255,15 +283,10 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        rank_barrier(world)
 
     def allmax(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(x, world, dev)
 
     w = WORKLOADS[WORKLOAD]
     inp = make_inputs(w, device=dev)
@@ -335,7 +358,7 @@ def run_ours(args):
     total_ms = ev[0].elapsed_time(ev[-1])
     total_ms_max = allmax(total_ms)
     ms_step = total_ms_max / args.steps
-    value = elems * args.steps * world / (total_ms_max / 1e3) / 1e9
+    value = weak_scaling_value(elems * args.steps, world, total_ms_max)
     kern_ms = statistics.mean(per_step)
     achieved_ex2 = exps / (kern_ms / 1e3) / 1e9
     achieved_gbs = alg_bytes / (kern_ms / 1e3) / 1e9
