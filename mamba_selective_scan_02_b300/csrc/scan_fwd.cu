@@ -406,16 +406,24 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     }
                 }
                 // ---- the recurrence over the block's 8 tokens.  Ā and B̄u of
-                // token j+1 are formed before the state of token j is updated.
+                // token j+1 are formed before the state of token j is updated,
+                // and the read-out C·h of token j runs after the update of token
+                // j+1, so the chains interleave.  The B row a token needs is
+                // loaded one iteration before it is used, the C row likewise.
+                constexpr int NR = SPT / 4;  // 16-byte words of a lane's B or C row
+                auto load_row = [&](const float *base, int j, float4 *r) {
+                    const float *row = base + (8 * blk + j) * S::BCP + SPT * g;
+#pragma unroll
+                    for (int q4 = 0; q4 < NR; ++q4) r[q4] = *reinterpret_cast<const float4 *>(row + 4 * q4);
+                };
                 float2 an[NQ], bn[NQ];
-                auto decay_input = [&](int j, float2 *ao, float2 *bo) {
+                auto decay_input = [&](int j, const float4 *br, float2 *ao, float2 *bo) {
                     const float dv = (j & 1) ? dl[j >> 1].y : dl[j >> 1].x;
                     const float uv = (j & 1) ? du[j >> 1].y : du[j >> 1].x;
                     const float2 d2 = make_float2(dv, dv), du2 = make_float2(uv, uv);
-                    const float *Brow = Bf + (8 * blk + j) * S::BCP + SPT * g;
 #pragma unroll
-                    for (int q4 = 0; q4 < SPT / 4; ++q4) {
-                        const float4 bq = *reinterpret_cast<const float4 *>(Brow + 4 * q4);
+                    for (int q4 = 0; q4 < NR; ++q4) {
+                        const float4 bq = br[q4];
                         const float2 x0 = __fmul2_rn(d2, A2[2 * q4]);
                         const float2 x1 = __fmul2_rn(d2, A2[2 * q4 + 1]);
                         ao[2 * q4] = make_float2(ex2(x0.x), ex2(x0.y));
@@ -431,17 +439,13 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                         }
                     }
                 };
-                decay_input(0, an, bn);
-                // The read-out C·h of token j runs after the state update of
-                // token j + 1, so the two chains interleave.
                 float p[8];
                 float2 hp[NQ];
-                auto readout = [&](int j, const float2 *hs) {
-                    const float *Crow = Cf + (8 * blk + j) * S::BCP + SPT * g;
+                auto readout = [&](int j, const float2 *hs, const float4 *cr) {
                     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int q4 = 0; q4 < SPT / 4; ++q4) {
-                        const float4 cq = *reinterpret_cast<const float4 *>(Crow + 4 * q4);
+                    for (int q4 = 0; q4 < NR; ++q4) {
+                        const float4 cq = cr[q4];
                         if (q4 == 0) {
                             acc0 = __fmul2_rn(make_float2(cq.x, cq.y), hs[0]);
                             acc1 = __fmul2_rn(make_float2(cq.z, cq.w), hs[1]);
@@ -453,6 +457,13 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     const float2 s2 = __fadd2_rn(acc0, acc1);
                     p[j] = s2.x + s2.y;
                 };
+                float4 Bnx[NR], Cnx[NR];
+                {
+                    float4 b0[NR];
+                    load_row(Bf, 0, b0);
+                    load_row(Bf, 1, Bnx);
+                    decay_input(0, b0, an, bn);
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     float2 ac[NQ], bc[NQ];
@@ -461,18 +472,25 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                         ac[q] = an[q];
                         bc[q] = bn[q];
                     }
-                    if (j < 7) decay_input(j + 1, an, bn);
+                    if (j < 7) {
+                        float4 bcur[NR];
+#pragma unroll
+                        for (int q4 = 0; q4 < NR; ++q4) bcur[q4] = Bnx[q4];
+                        if (j < 6) load_row(Bf, j + 2, Bnx);
+                        decay_input(j + 1, bcur, an, bn);
+                    }
 #pragma unroll
                     for (int q = 0; q < NQ; ++q) h[q] = __ffma2_rn(ac[q], h[q], bc[q]);
                     if (MODE == 0) {
-                        if (j > 0) readout(j - 1, hp);
+                        if (j > 0) readout(j - 1, hp, Cnx);
+                        load_row(Cf, j, Cnx);
 #pragma unroll
                         for (int q = 0; q < NQ; ++q) hp[q] = h[q];
                     } else {
                         dsum += (j & 1) ? dl[j >> 1].y : dl[j >> 1].x;
                     }
                 }
-                if (MODE == 0) readout(7, hp);
+                if (MODE == 0) readout(7, hp, Cnx);
                 if (MODE == 0) {
                     if (NG == 1) {
                         float y[8];
