@@ -307,8 +307,8 @@ def run_ours(args):
         flush_w.zero_()
         flush_r.sum()
     plan = capi.ssm_scan_plan(p)
-    # one scan kernel, or aggregate + carry + scan kernels in two-pass mode
-    launches_per_step = 1 if (plan["chained"] or plan["nchunks"] == 1) else 3
+    # B/C widening + scan, or widening + aggregate + carry + scan in two-pass mode
+    launches_per_step = 2 if (plan["chained"] or plan["nchunks"] == 1) else 4
 
     # MUFU ex2 peak, measured on this GPU (the roofline's exponential side)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count

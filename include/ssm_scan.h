@@ -97,9 +97,10 @@ size_t ssm_scan_workspace_size(const ssm_scan_params *p);
 /* How ssm_scan_fwd will cut this scan into work items (host-side, no GPU
  * needed).  On SSM_OK fills out[0] = tokens per chunk, out[1] = number of
  * chunks K, out[2] = 1 if chunk k starts from the state chunk k-1 hands over
- * (one kernel launch) or 0 if an aggregate pass and a carry pass precompute the
+ * (one scan launch) or 0 if an aggregate pass and a carry pass precompute the
  * chunks' starting states (three launches when K > 1), out[3] = number of
- * channel groups (one warp each).  Returns SSM_ERR_INVALID_ARG for invalid
+ * channel groups (one warp each).  Every scan is preceded by one small launch
+ * that widens B and C to fp32 token-major rows in the workspace.  Returns SSM_ERR_INVALID_ARG for invalid
  * sizes or a NULL out. */
 ssm_status ssm_scan_plan(const ssm_scan_params *p, int64_t out[4]);
 

@@ -17,7 +17,7 @@ inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3
 
 struct Layout {
     ssm::ScanPlan plan;
-    size_t flags_off, agg_off, carry_off, zero_bytes, total;
+    size_t flags_off, agg_off, carry_off, bt_off, ct_off, zero_bytes, total;
 };
 
 bool scan_sizes_ok(const ssm_scan_params *p) {
@@ -31,7 +31,8 @@ bool scan_sizes_ok(const ssm_scan_params *p) {
 // Workspace: a 256-byte header (status word, two work counters), then
 //   chained:  one int flag per channel group, and one b × D × N fp32 state;
 //   two-pass: per-chunk aggregates [b][D][K-1][N] (float2) and carried states
-//             [b][D][K][N] (fp32).
+//             [b][D][K][N] (fp32);
+// then, always, B and C widened to fp32 token-major rows [b][L][np].
 // The header and the flags are cleared before every launch.
 Layout scan_layout(const ssm_scan_params *p) {
     Layout l;
@@ -50,6 +51,10 @@ Layout scan_layout(const ssm_scan_params *p) {
         l.carry_off = kHeader + agg_bytes;
         l.total = l.carry_off + align256(bdn * (size_t)l.plan.nchunks * sizeof(float));
     }
+    const size_t bt_bytes = align256((size_t)p->batch * p->seqlen * l.plan.np * sizeof(float));
+    l.bt_off = l.total;
+    l.ct_off = l.bt_off + bt_bytes;
+    l.total = l.ct_off + bt_bytes;
     return l;
 }
 
@@ -132,6 +137,9 @@ ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream) {
     a.nchunks = (int)l.plan.nchunks;
     a.groups = (int)l.plan.groups;
     a.chained = l.plan.chained ? 1 : 0;
+    a.Bt = reinterpret_cast<float *>(ws + l.bt_off);
+    a.Ct = reinterpret_cast<float *>(ws + l.ct_off);
+    a.np = l.plan.np;
     return ssm::scan_launch(a, p->io_dtype == SSM_BF16, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

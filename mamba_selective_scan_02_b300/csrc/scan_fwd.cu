@@ -70,16 +70,13 @@ template <typename T, int SPT, int NG> struct WTile {
     static constexpr int NB8 = kTT / 8;           // 8-token blocks per tile
     static constexpr int BLK = CPW * 8 * ES;      // one 8-token block of one input
     static constexpr int SEQ = NB8 * BLK;         // one input tile
-    static constexpr int BC = NP * kTT * ES;      // one B or C tile (N <= NP rows)
-    static constexpr int BCP = NP + 4;            // fp32 B/C row pitch in floats (16-B rows)
+    static constexpr int BC = kTT * NP * 4;       // one fp32 B or C tile, token-major rows of NP
     static constexpr int BUF = 3 * al128(SEQ) + 2 * al128(BC);  // one stage: u, Δ, z, B, C
     static constexpr int off_u = 0, off_d = al128(SEQ), off_z = 2 * al128(SEQ);
     static constexpr int off_B = 3 * al128(SEQ), off_C = off_B + al128(BC);
     static constexpr int OUT = al128(SEQ);                       // one y tile
     static constexpr int off_out = 2 * BUF;                      // two y tiles
-    static constexpr int off_Bf = off_out + 2 * OUT;
-    static constexpr int off_Cf = off_Bf + al128(kTT * BCP * 4);
-    static constexpr int off_ex = off_Cf + al128(kTT * BCP * 4);  // (Δ, Δ·u) of one 8-token block
+    static constexpr int off_ex = off_out + 2 * OUT;             // (Δ, Δ·u) of one 8-token block
     static constexpr int off_bar = off_ex + al128(CPW * 5 * 16);  // 5 slots per channel: 4 + 1 pad
     static constexpr int bytes = off_bar + 16;
 };
@@ -138,8 +135,6 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     constexpr int CPW = S::CPW, NB8 = S::NB8, NQ = SPT / 2;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(128) unsigned char smem[];
-    float *Bf = reinterpret_cast<float *>(smem + S::off_Bf);
-    float *Cf = reinterpret_cast<float *>(smem + S::off_Cf);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::off_bar);
 
     const int lane = threadIdx.x;
@@ -179,7 +174,7 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     }
     __syncwarp();
 
-    const uint32_t bc_bytes = (uint32_t)N * kTT * sizeof(T);
+    constexpr uint32_t bc_bytes = S::BC;
     auto stage = [&](int s) { return smem + s * S::BUF; };
     auto issue_loads = [&](const Item &it, int tile, int s) {
         const int t0 = it.t_begin + tile * kTT;
@@ -192,8 +187,8 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             tma_load_3d(st + S::off_d + j * S::BLK, &maps.d, &bar[s], t0 + 8 * j, it.d0, it.b);
             if (MODE == 0 && HAS_Z) tma_load_3d(st + S::off_z + j * S::BLK, &maps.z, &bar[s], t0 + 8 * j, it.d0, it.b);
         }
-        tma_load_3d(st + S::off_B, &maps.B, &bar[s], t0, 0, it.b);
-        if (MODE == 0) tma_load_3d(st + S::off_C, &maps.C, &bar[s], t0, 0, it.b);
+        tma_load_3d(st + S::off_B, &maps.B, &bar[s], 0, t0, it.b);
+        if (MODE == 0) tma_load_3d(st + S::off_C, &maps.C, &bar[s], 0, t0, it.b);
     };
     // Plain loads for shapes TMA cannot describe (row pitch not a multiple of 16 B).
     auto generic_loads = [&](const Item &it, int tile, int s) {
@@ -212,14 +207,13 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             ds[si] = in ? gdl[off] : T(0.f);
             if (MODE == 0 && HAS_Z) zs[si] = in ? gz[off] : T(0.f);
         }
-        T *Bs = reinterpret_cast<T *>(st + S::off_B), *Cs = reinterpret_cast<T *>(st + S::off_C);
-        const T *gB = static_cast<const T *>(a.B), *gC = static_cast<const T *>(a.C);
-        for (int i = lane; i < N * kTT; i += 32) {
-            const int n = i / kTT, tt = i % kTT, t = t0 + tt;
+        float *Bs = reinterpret_cast<float *>(st + S::off_B), *Cs = reinterpret_cast<float *>(st + S::off_C);
+        for (int i = lane; i < kTT * S::NP; i += 32) {
+            const int tt = i / S::NP, t = t0 + tt;
             const bool in = t < L;
-            const size_t off = ((size_t)it.b * N + n) * L + t;
-            Bs[i] = in ? gB[off] : T(0.f);
-            if (MODE == 0) Cs[i] = in ? gC[off] : T(0.f);
+            const size_t off = ((size_t)it.b * L + t) * S::NP + i % S::NP;
+            Bs[i] = in ? a.Bt[off] : 0.f;
+            if (MODE == 0) Cs[i] = in ? a.Ct[off] : 0.f;
         }
     };
 
@@ -306,35 +300,13 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 __syncwarp();
             }
 
-            // ---- B (and C) widened to fp32, token-major rows, in 4 × 4 blocks
-            {
-                constexpr int NB = S::NP / 4, TB = kTT / 4;
-                constexpr int UNITS = (MODE == 0 ? 2 : 1) * NB * TB;
-                const T *Bs = reinterpret_cast<const T *>(st + S::off_B);
-                const T *Cs = reinterpret_cast<const T *>(st + S::off_C);
-                for (int u = lane; u < UNITS; u += 32) {
-                    const int mat = u / (NB * TB), r = u % (NB * TB);
-                    const int nb = r / TB, tb = r % TB;
-                    const T *src = mat ? Cs : Bs;
-                    float *dst = mat ? Cf : Bf;
-                    float4 v[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int n = 4 * nb + i;
-                        v[i] = n < N ? IO<T>::load4(src + n * kTT + 4 * tb) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                    float *row = dst + (4 * tb) * S::BCP + 4 * nb;
-                    *reinterpret_cast<float4 *>(row) = make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
-                    *reinterpret_cast<float4 *>(row + S::BCP) = make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
-                    *reinterpret_cast<float4 *>(row + 2 * S::BCP) = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
-                    *reinterpret_cast<float4 *>(row + 3 * S::BCP) = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
-                }
-            }
             // The y tile written two tiles ago must have left shared memory.
             if (TMA && MODE == 0 && lane == 0) bulk_wait_read1();
             __syncwarp();
 
             T *out = reinterpret_cast<T *>(smem + S::off_out + ostage * S::OUT);
+            const float *Bf = reinterpret_cast<const float *>(st + S::off_B);
+            const float *Cf = reinterpret_cast<const float *>(st + S::off_C);
             const T *u_t = reinterpret_cast<const T *>(st + S::off_u);
             const T *d_t = reinterpret_cast<const T *>(st + S::off_d);
             const T *z_t = reinterpret_cast<const T *>(st + S::off_z);
@@ -412,7 +384,7 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 // loaded one iteration before it is used, the C row likewise.
                 constexpr int NR = SPT / 4;  // 16-byte words of a lane's B or C row
                 auto load_row = [&](const float *base, int j, float4 *r) {
-                    const float *row = base + (8 * blk + j) * S::BCP + SPT * g;
+                    const float *row = base + (8 * blk + j) * S::NP + SPT * g;
 #pragma unroll
                     for (int q4 = 0; q4 < NR; ++q4) r[q4] = *reinterpret_cast<const float4 *>(row + 4 * q4);
                 };
@@ -587,6 +559,29 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     if (TMA && MODE == 0 && lane == 0) bulk_wait0();
 }
 
+// B and C, [b][N][L] in the I/O type, widened once per launch to fp32
+// token-major rows [b][L][np] (zero for n >= N), the layout every warp's TMA
+// loads take per tile.  One block per (32 tokens, sequence), staged through
+// shared memory so reads and writes are both coalesced.
+template <typename T>
+__global__ void __launch_bounds__(256) widen_bc_kernel(const ScanArgs a) {
+    __shared__ float tile[2][16][33];
+    const int b = blockIdx.y, t0 = blockIdx.x * 32, N = a.dstate, L = a.seqlen, np = a.np;
+    const T *B = static_cast<const T *>(a.B) + (size_t)b * N * L;
+    const T *C = static_cast<const T *>(a.C) + (size_t)b * N * L;
+    for (int i = threadIdx.x; i < 2 * 16 * 32; i += blockDim.x) {
+        const int m = i / (16 * 32), n = (i / 32) % 16, tt = i % 32, t = t0 + tt;
+        float v = 0.f;
+        if (n < N && t < L) v = IO<T>::to_f((m ? C : B)[(size_t)n * L + t]);
+        tile[m][n][tt] = v;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 2 * 32 * np; i += blockDim.x) {
+        const int m = i / (32 * np), tt = (i / np) % 32, n = i % np, t = t0 + tt;
+        if (t < L) (m ? a.Ct : a.Bt)[((size_t)b * L + t) * np + n] = tile[m][n][tt];
+    }
+}
+
 // Chains the chunk aggregates from h0 (two-pass mode): carry[0] = h0 and
 // carry[k+1] = P_k · carry[k] + S_k, the state chunk k+1 starts from.
 // One thread per (b, d, n).
@@ -677,6 +672,9 @@ cudaError_t launch_one(const Maps &maps, const ScanArgs &a, int items, cudaStrea
 template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, bool ZOH>
 cudaError_t launch_all(const Maps &maps, const ScanArgs &a, cudaStream_t st) {
     cudaError_t e;
+    widen_bc_kernel<T><<<dim3((a.seqlen + 31) / 32, a.batch), 256, 0, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     if (a.nchunks > 1 && !a.chained) {
         e = launch_one<T, SPT, NG, false, TMA, 1, ZOH>(maps, a, a.groups * (a.nchunks - 1), st);
         if (e != cudaSuccess) return e;
@@ -721,6 +719,7 @@ int scan_groups(int64_t dstate) { return dstate <= 4 ? 1 : (dstate <= 8 ? 2 : 4)
 ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t requested) {
     ScanPlan p;
     const Split sp = split_for(dstate);
+    p.np = sp.spt * sp.ng;
     p.cpw = 32 / sp.ng;
     p.groups = batch * ((dim + p.cpw - 1) / p.cpw);
     const int64_t resident = (int64_t)kSMs * kWarpsPerSM;
@@ -756,8 +755,8 @@ cudaError_t scan_launch(const ScanArgs &a, bool bf16, cudaStream_t st) {
         const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
         bool ok = make_map(&maps.u, dt, es, a.u, a.seqlen, a.dim, a.batch, 8, cpw) &&
                   make_map(&maps.d, dt, es, a.delta, a.seqlen, a.dim, a.batch, 8, cpw) &&
-                  make_map(&maps.B, dt, es, a.B, a.seqlen, a.dstate, a.batch, kTT, a.dstate) &&
-                  make_map(&maps.C, dt, es, a.C, a.seqlen, a.dstate, a.batch, kTT, a.dstate) &&
+                  make_map(&maps.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.Bt, a.np, a.seqlen, a.batch, a.np, kTT) &&
+                  make_map(&maps.C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.Ct, a.np, a.seqlen, a.batch, a.np, kTT) &&
                   make_map(&maps.y, dt, es, a.y, a.seqlen, a.dim, a.batch, 8, cpw);
         if (ok && a.z) ok = make_map(&maps.z, dt, es, a.z, a.seqlen, a.dim, a.batch, 8, cpw);
         if (!ok) return cudaErrorInvalidValue;

@@ -25,6 +25,8 @@ struct ScanArgs {
     int nchunks;     // K
     int groups;      // channel groups: batch × ceil(dim / channels per warp)
     int chained;     // 1: chunk k waits for chunk k-1's state; 0: two-pass carries
+    float *Bt, *Ct;  // B and C widened to fp32, token-major: [b][L][np], zero beyond N
+    int np;          // states per token row of Bt / Ct (N rounded up to 4, 8 or 16)
 };
 
 // How a scan is cut into work items.  One warp owns a group of channels for
@@ -33,6 +35,7 @@ struct ScanArgs {
 // Two-pass: an aggregate pass and a carry pass precompute every chunk's
 // starting state so that all chunks run at once (few groups, long sequences).
 struct ScanPlan {
+    int np;             // B / C row length after widening (N rounded up to 4, 8 or 16)
     int cpw;            // channels per warp
     int64_t groups;     // batch × ceil(dim / cpw)
     bool chained;

@@ -90,26 +90,31 @@ def test_scan_rejects_null_params():
     assert capi.lib().ssm_scan_workspace_size(None) == 0
 
 
+def _bc_bytes(b, L, np_):
+    """B and C widened to fp32 token-major rows: two [b][L][np] arrays."""
+    return 2 * (-(-b * L * np_ * 4 // 256) * 256)
+
+
 def test_workspace_size():
     p = valid_scan(chunk_len=0)
-    assert capi.ssm_scan_workspace_size(p) == 256          # one chunk: status word only
-    p = valid_scan(chunk_len=64)                             # 4 chunks of 64 tokens
+    assert capi.ssm_scan_workspace_size(p) == 256 + _bc_bytes(2, 256, 16)   # one chunk
+    p = valid_scan(chunk_len=64)                             # 4 chunks of 64 tokens, two-pass
     bdn = 2 * 64 * 16
     agg = -(-bdn * 3 * 8 // 256) * 256
     carry = -(-bdn * 4 * 4 // 256) * 256
-    assert capi.ssm_scan_workspace_size(p) == 256 + agg + carry
+    assert capi.ssm_scan_workspace_size(p) == 256 + agg + carry + _bc_bytes(2, 256, 16)
     # the small-model layer shape is split into chunks automatically
     p = valid_scan(batch=2, dim=1536, seqlen=2048)
-    assert capi.ssm_scan_workspace_size(p) > 256
+    assert capi.ssm_scan_workspace_size(p) > 256 + _bc_bytes(2, 2048, 16)
     # enough channel groups to fill the GPU: chunks are chained, and the
     # workspace holds one flag per group of 16 channels and one hand-off state
     p = valid_scan(batch=4, dim=5120, seqlen=2048)
     groups = 4 * 5120 // 16
     flags = -(-groups * 4 // 256) * 256
-    assert capi.ssm_scan_workspace_size(p) == 256 + flags + 4 * 5120 * 16 * 4
-    # a single chunk needs the header only
-    p = valid_scan(batch=1, dim=64, seqlen=256)
-    assert capi.ssm_scan_workspace_size(p) == 256
+    assert capi.ssm_scan_workspace_size(p) == 256 + flags + 4 * 5120 * 16 * 4 + _bc_bytes(4, 2048, 16)
+    # small state sizes widen B and C to rows of 4 or 8
+    p = valid_scan(batch=1, dim=64, dstate=4, seqlen=256)
+    assert capi.ssm_scan_workspace_size(p) == 256 + _bc_bytes(1, 256, 4)
     # too small a workspace is rejected
     p = valid_scan(chunk_len=64, workspace_bytes=300)
     assert capi.ssm_scan_fwd(p, None) == capi.SSM_ERR_INVALID_ARG
