@@ -732,11 +732,25 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
     } else if (requested > 0) {
         p.chunk_len = std::min<int64_t>(requested, Lr);
     } else {
-        // Split the sequence until the items fill the resident warps.
-        int64_t K = (resident + p.groups - 1) / p.groups;
-        K = std::max<int64_t>(1, std::min<int64_t>(K, (seqlen + 511) / 512));
-        const int64_t len = (seqlen + K - 1) / K;
-        p.chunk_len = ((len + 63) / 64) * 64;
+        // Two-pass: pick the chunk length whose passes take the fewest rounds of
+        // resident warps × tokens per round.  A pass over n items takes
+        // ceil(n / resident) rounds of one chunk each; the aggregate pass costs
+        // about 0.7 of a main-pass chunk (no read-out, no output).  A single
+        // chunk (no aggregate pass) is one of the candidates.  Splitting adds
+        // two launches (aggregate, carry), charged as 64 tokens of one round.
+        double best = 1e300;
+        p.chunk_len = Lr;
+        for (int64_t len = Lr; len >= 64; len -= 64) {
+            const int64_t K = (seqlen + len - 1) / len;
+            if (K > 64) break;
+            const int64_t rm = (p.groups * K + resident - 1) / resident;
+            const int64_t ra = (p.groups * (K - 1) + resident - 1) / resident;
+            const double cost = (double)len * ((double)rm + 0.7 * (double)ra) + (K > 1 ? 64.0 : 0.0);
+            if (cost < best * 0.999) {
+                best = cost;
+                p.chunk_len = len;
+            }
+        }
     }
     p.nchunks = (seqlen + p.chunk_len - 1) / p.chunk_len;
     if (p.nchunks == 1) p.chained = false;

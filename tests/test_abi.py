@@ -96,7 +96,7 @@ def _bc_bytes(b, L, np_):
 
 
 def test_workspace_size():
-    p = valid_scan(chunk_len=0)
+    p = valid_scan(chunk_len=256)
     assert capi.ssm_scan_workspace_size(p) == 256 + _bc_bytes(2, 256, 16)   # one chunk
     p = valid_scan(chunk_len=64)                             # 4 chunks of 64 tokens, two-pass
     bdn = 2 * 64 * 16
@@ -113,7 +113,7 @@ def test_workspace_size():
     flags = -(-groups * 4 // 256) * 256
     assert capi.ssm_scan_workspace_size(p) == 256 + flags + 4 * 5120 * 16 * 4 + _bc_bytes(4, 2048, 16)
     # small state sizes widen B and C to rows of 4 or 8
-    p = valid_scan(batch=1, dim=64, dstate=4, seqlen=256)
+    p = valid_scan(batch=1, dim=64, dstate=4, seqlen=256, chunk_len=256)
     assert capi.ssm_scan_workspace_size(p) == 256 + _bc_bytes(1, 256, 4)
     # too small a workspace is rejected
     p = valid_scan(chunk_len=64, workspace_bytes=300)
@@ -125,8 +125,12 @@ def test_scan_plan():
     assert plan == {"chunk_len": 256, "nchunks": 8, "chained": True, "groups": 1280}
     plan = capi.ssm_scan_plan(valid_scan(batch=1, dim=5120, seqlen=131072))
     assert not plan["chained"] and plan["nchunks"] > 1 and plan["chunk_len"] % 64 == 0
-    plan = capi.ssm_scan_plan(valid_scan(batch=1, dim=64, seqlen=256))
+    plan = capi.ssm_scan_plan(valid_scan(batch=1, dim=64, seqlen=64))
     assert plan["nchunks"] == 1 and not plan["chained"]
+    # few channel groups on a long sequence: chunks sized so that both passes
+    # fill the resident warps (320 groups, 131072 tokens -> dozens of chunks)
+    plan = capi.ssm_scan_plan(valid_scan(batch=1, dim=5120, seqlen=131072))
+    assert plan["nchunks"] * plan["groups"] >= 8 * 1184
     assert capi.lib().ssm_scan_plan(None, None) == capi.SSM_ERR_INVALID_ARG
 
 
