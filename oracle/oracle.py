@@ -52,6 +52,10 @@ def _bind(lib):
     lib.oracle_scan.argtypes = [_I64, _I64, _I64, _I64,
                                 _D, _D, _D, _D, _D, _D, _D, _D,
                                 ctypes.c_int, ctypes.c_int, _D, _D, _D, _I64, _I64]
+    lib.oracle_conv1d.restype = ctypes.c_int
+    lib.oracle_conv1d.argtypes = [_I64, _I64, _I64, _I64, _D, _D, _D, ctypes.c_int, _D, _D, _D]
+    lib.oracle_conv1d_step.restype = ctypes.c_int
+    lib.oracle_conv1d_step.argtypes = [_I64, _I64, _I64, _D, _D, _D, _D, ctypes.c_int, _D]
     lib.oracle_step.restype = ctypes.c_int
     lib.oracle_step.argtypes = [_I64, _I64, _I64,
                                 _D, _D, _D, _D, _D, _D, _D, _D, _D,
@@ -140,3 +144,38 @@ def step(state, u, delta, A, B, C, Dskip=None, z=None, bias=None,
     if rc != 0:
         raise RuntimeError("oracle_step failed")
     return y, st
+
+
+def conv1d(x, w, bias=None, state_in=None, silu=True, lib=None):
+    """Causal depthwise convolution (+ bias, + SiLU).  x: (b, D, L); w: (D, W);
+    bias: (D,); state_in: (b, D, W-1), oldest first.  Returns (u (b, D, L),
+    state_out (b, D, W-1)) in fp64."""
+    lib = lib or load()
+    x, w, bias, state_in = map(_f64, (x, w, bias, state_in))
+    b, dim, L = x.shape
+    W = w.shape[1]
+    assert w.shape == (dim, W) and (state_in is None or state_in.shape == (b, dim, W - 1))
+    u = np.empty((b, dim, L), np.float64)
+    st = np.empty((b, dim, W - 1), np.float64)
+    rc = lib.oracle_conv1d(b, dim, L, W, _p(x), _p(w), _p(bias), int(bool(silu)),
+                           _p(state_in), _p(u), _p(st))
+    if rc != 0:
+        raise RuntimeError("oracle_conv1d failed")
+    return u, st
+
+
+def conv1d_step(state, x, w, bias=None, silu=True, lib=None):
+    """One decode token of the convolution.  state: (b, D, W-1) fp64, updated in
+    place (a new array is returned if it was not contiguous float64 numpy);
+    x: (b, D).  Returns (u (b, D), state)."""
+    lib = lib or load()
+    st = _f64(state)
+    x, w, bias = map(_f64, (x, w, bias))
+    b, dim = x.shape
+    W = w.shape[1]
+    assert st.shape == (b, dim, W - 1) and w.shape == (dim, W)
+    u = np.empty((b, dim), np.float64)
+    rc = lib.oracle_conv1d_step(b, dim, W, _p(st), _p(x), _p(w), _p(bias), int(bool(silu)), _p(u))
+    if rc != 0:
+        raise RuntimeError("oracle_conv1d_step failed")
+    return u, st

@@ -39,9 +39,27 @@
  *     log1p(e^x) otherwise;
  *   - the bias is one value per channel, added before the softplus.
  *
+ * The short convolution in front of the SSM (oracle_conv1d, oracle_conv1d_step):
+ *   u_t = silu(bias + Σ_{k=0}^{W−1} w_k · x_{t−(W−1)+k})
+ *           [a causal depthwise convolution of width 4, then SiLU, feeds the
+ *           SSM branch: first-principles page — "The Mamba block"; erikxu.me
+ *           notes — "Mamba Architecture"; the per-channel bias and width 4
+ *           follow from the per-layer weight count on the first-principles
+ *           page, "The Mamba block", which only adds up with D·4 + D
+ *           convolution weights]
+ *   inputs before the sequence come from a carried state of the last W−1
+ *   inputs, oldest first (zeros when none) [three numbers per channel in the
+ *   state count of "A fixed state against a growing cache" / "What a fixed
+ *   state is bad at" on the same page].
+ * Reading taken: tap k = W−1 multiplies the current input (the taps are the
+ * filter in time order, oldest first); SiLU is optional so the plain
+ * convolution can be checked on its own.
+ *
  * Parity is pinned by tests/test_oracle_pins.py (worked example, convolution
  * kernel, gated-RNN reduction, Δ limits, first output, product-form brute
- * force, continuation) and tests/test_oracle_mutants.py (planted mistakes
+ * force, continuation; for the short convolution: numpy's convolution, the
+ * impulse response, split and decode continuation, and the printed Mamba-2.8B
+ * weight and state totals) and tests/test_oracle_mutants.py (planted mistakes
  * must fail a pin).
  *
  * Layouts (all row-major, fp64):
@@ -173,6 +191,79 @@ int oracle_step(int64_t batch, int64_t dim, int64_t dstate,
                 out *= oracle_silu(z[c]);
             y[c] = out;
         }
+    }
+    return 0;
+}
+
+/*
+ * Causal depthwise convolution + bias + optional SiLU over a whole sequence,
+ * for every channel c = (b, d).
+ *   x, u      : batch × dim × seqlen (time fastest)
+ *   w         : dim × width (tap width−1 multiplies the current input)
+ *   bias      : dim, may be NULL (zero)
+ *   state_in  : batch × dim × (width−1), the inputs just before x[.., 0],
+ *               oldest first; NULL = zeros
+ *   state_out : batch × dim × (width−1), the last width−1 inputs of the
+ *               sequence (reaching into state_in when seqlen < width−1),
+ *               oldest first; NULL = not written.  Must not overlap state_in.
+ * Returns 0, or -1 if width < 1.
+ */
+int oracle_conv1d(int64_t batch, int64_t dim, int64_t seqlen, int64_t width,
+                  const double *x, const double *w, const double *bias, int silu,
+                  const double *state_in, double *u, double *state_out)
+{
+    if (width < 1)
+        return -1;
+    const int64_t hist = width - 1;
+    for (int64_t c = 0; c < batch * dim; ++c) {
+        const int64_t d = c % dim;
+        const double *x_c = x + c * seqlen;
+        const double *s_c = state_in ? state_in + c * hist : NULL;
+        /* the input at time s, reaching back into the carried state for s < 0 */
+#define ORACLE_X_AT(s) ((s) >= 0 ? x_c[(s)] : (s_c ? s_c[hist + (s)] : 0.0))
+        for (int64_t t = 0; t < seqlen; ++t) {
+            double acc = bias ? bias[d] : 0.0;
+            for (int64_t k = 0; k < width; ++k) {
+                const int64_t s = t - hist + k;
+                acc += w[d * width + k] * ORACLE_X_AT(s);
+            }
+            u[c * seqlen + t] = silu ? oracle_silu(acc) : acc;
+        }
+        if (state_out)
+            for (int64_t j = 0; j < hist; ++j) {
+                const int64_t s = seqlen - hist + j;
+                state_out[c * hist + j] = ORACLE_X_AT(s);
+            }
+#undef ORACLE_X_AT
+    }
+    return 0;
+}
+
+/*
+ * One decode token of the same convolution: the window is the carried state
+ * (width−1 inputs, oldest first) followed by this token's input; the state
+ * then drops its oldest input and appends this one, in place.
+ *   state : batch × dim × (width−1)     x, u : batch × dim
+ */
+int oracle_conv1d_step(int64_t batch, int64_t dim, int64_t width, double *state,
+                       const double *x, const double *w, const double *bias, int silu,
+                       double *u)
+{
+    if (width < 1)
+        return -1;
+    const int64_t hist = width - 1;
+    for (int64_t c = 0; c < batch * dim; ++c) {
+        const int64_t d = c % dim;
+        double *s_c = state + c * hist;
+        double acc = bias ? bias[d] : 0.0;
+        for (int64_t k = 0; k < hist; ++k)
+            acc += w[d * width + k] * s_c[k];
+        acc += w[d * width + hist] * x[c];
+        u[c] = silu ? oracle_silu(acc) : acc;
+        for (int64_t k = 0; k + 1 < hist; ++k)
+            s_c[k] = s_c[k + 1];
+        if (hist > 0)
+            s_c[hist - 1] = x[c];
     }
     return 0;
 }

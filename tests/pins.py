@@ -305,5 +305,110 @@ def pin_decode_equals_scan(lib, seed=17):
         _close(st, hL, 1e-13, 1e-15, f"decode carried state (zoh={zoh})")
 
 
+# --------------------------------------------------------------------------
+# P8: the short convolution in front of the SSM (first-principles page — "The
+# Mamba block"; erikxu.me notes — "Mamba Architecture") is a causal FIR filter
+# per channel: with no SiLU it is numpy's full convolution of the carried
+# inputs followed by the sequence with the taps in reverse, cut to the
+# sequence's positions, plus the bias; with SiLU it is that value times its
+# logistic sigmoid.  The final state is the last W−1 inputs.
+
+def pin_conv_library(lib, seed=18):
+    rng = np.random.default_rng(seed)
+    b, dim = 2, 3
+    for W in (1, 2, 3, 4):
+        for L in (1, 2, 5, 17):
+            x = rng.normal(size=(b, dim, L))
+            w = rng.normal(size=(dim, W))
+            bias = rng.normal(size=dim)
+            for st0 in (None, rng.normal(size=(b, dim, W - 1))):
+                hist = np.zeros((b, dim, W - 1)) if st0 is None else st0
+                full = np.concatenate([hist, x], axis=2)
+                want = np.zeros((b, dim, L))
+                for bi in range(b):
+                    for d in range(dim):
+                        want[bi, d] = np.convolve(full[bi, d], w[d][::-1])[W - 1:W - 1 + L] + bias[d]
+                for silu in (False, True):
+                    u, st = orc.conv1d(x, w, bias=bias, state_in=st0, silu=silu, lib=lib)
+                    _close(u, _silu(want) if silu else want, 1e-13, 1e-14,
+                           f"conv W={W} L={L} silu={silu} state={st0 is not None}")
+                    _close(st, full[..., full.shape[2] - (W - 1):], 0, 0, f"conv state W={W} L={L}")
+
+
+# P9: the taps in time order, oldest first: an impulse at τ comes out as the
+# taps reversed, w_{W−1} at τ, w_{W−2} at τ+1, … — and nothing before τ.
+
+def pin_conv_impulse(lib, seed=19):
+    rng = np.random.default_rng(seed)
+    W, L, tau = 4, 12, 5
+    w = rng.normal(size=(1, W))
+    x = np.zeros((1, 1, L))
+    x[0, 0, tau] = 1.0
+    u, _ = orc.conv1d(x, w, silu=False, lib=lib)
+    want = np.zeros(L)
+    for lag in range(W):
+        want[tau + lag] = w[0, W - 1 - lag]
+    _close(u[0, 0], want, 0, 0, "conv impulse response")
+    # an impulse carried in the state at position j (oldest first) is the
+    # input at time j − (W−1)
+    for j in range(W - 1):
+        st = np.zeros((1, 1, W - 1))
+        st[0, 0, j] = 1.0
+        u, _ = orc.conv1d(np.zeros((1, 1, L)), w, state_in=st, silu=False, lib=lib)
+        want = np.zeros(L)
+        for t in range(L):
+            k = (j - (W - 1)) - t + (W - 1)  # tap that sees time j−(W−1) at output t
+            if 0 <= k < W:
+                want[t] = w[0, k]
+        _close(u[0, 0], want, 0, 0, f"conv state impulse {j}")
+
+
+# P10: the convolution state carries across any split of the sequence, and W−1
+# inputs are all it needs: the sequence form equals one decode step per token.
+
+def pin_conv_continuation(lib, seed=20):
+    rng = np.random.default_rng(seed)
+    b, dim, L = 2, 3, 23
+    for W in (1, 2, 4):
+        x = rng.normal(size=(b, dim, L))
+        w = rng.normal(size=(dim, W))
+        bias = rng.normal(size=dim)
+        st0 = rng.normal(size=(b, dim, W - 1))
+        u, st = orc.conv1d(x, w, bias=bias, state_in=st0, lib=lib)
+        for cut in (1, 2, 11):
+            ua, sa = orc.conv1d(x[..., :cut], w, bias=bias, state_in=st0, lib=lib)
+            ub, sb = orc.conv1d(x[..., cut:], w, bias=bias, state_in=sa, lib=lib)
+            _close(np.concatenate([ua, ub], -1), u, 1e-15, 1e-15, f"conv split at {cut}, W={W}")
+            _close(sb, st, 0, 0, f"conv state after split at {cut}, W={W}")
+        s = st0.copy()
+        for t in range(L):
+            ut, s = orc.conv1d_step(s, x[..., t], w, bias=bias, lib=lib)
+            _close(ut, u[..., t], 1e-15, 1e-15, f"conv decode token {t}, W={W}")
+        _close(s, st, 0, 0, f"conv decode state, W={W}")
+
+
+# P11: the block's shapes against the totals printed for Mamba-2.8B
+# (tests/golden/mamba28b_counts.txt).  A convolution of width 4 with one bias
+# per channel is what makes the per-layer weights add up to the printed model
+# total, and a state of W−1 = 3 inputs per channel, next to N = 16 SSM states,
+# is what makes the printed whole-state size; the state length is taken from
+# the oracle's own output.
+
+def pin_block_counts(lib):
+    g = {k: int(v[0]) for k, v in read_golden("mamba28b_counts.txt").items()}
+    dm, E, N, R, W = g["d_model"], g["inner"], g["dstate"], g["dt_rank"], g["conv_width"]
+    ssm = E * (R + 2 * N) + (R * E + E) + E * N + E        # x_proj, dt_proj (+bias), A, D
+    assert ssm == g["ssm_weights_per_layer"]
+    assert E * N == g["state_entries_per_layer"]
+    conv = E * W + E                                       # depthwise taps + one bias per channel
+    layer = dm * 2 * E + conv + ssm + E * dm + dm          # in_proj, conv, SSM, out_proj, norm
+    assert g["layers"] * layer + g["vocab"] * dm + dm == g["total_weights"]
+    _, st = orc.conv1d(np.zeros((1, 1, 5)), np.ones((1, W)), silu=False, lib=lib)
+    per_channel_conv_state = st.shape[2]
+    assert g["layers"] * E * (N + per_channel_conv_state) == g["whole_state"]
+    assert g["pythia_tokens"] * 2 * g["pythia_layers"] * dm == g["whole_state"]
+
+
 ALL_PINS = [pin_worked_example, pin_lti_convolution, pin_gated_rnn, pin_delta_limits,
-            pin_first_output, pin_product_form, pin_continuation, pin_decode_equals_scan]
+            pin_first_output, pin_product_form, pin_continuation, pin_decode_equals_scan,
+            pin_conv_library, pin_conv_impulse, pin_conv_continuation, pin_block_counts]

@@ -39,6 +39,17 @@ MUTANTS = {
     "step_state_not_decayed": ("*h = abar * *h + bbar * u[c];", "*h = *h + bbar * u[c];"),
     "step_B_of_batch_0": ("oracle_bbar(dt, a, B[b * dstate + n], zoh)", "oracle_bbar(dt, a, B[n], zoh)"),
     "step_no_bias": ("double dt = delta[c] + (bias ? bias[d] : 0.0);", "double dt = delta[c];"),
+    "conv_taps_reversed": ("acc += w[d * width + k] * ORACLE_X_AT(s);",
+                           "acc += w[d * width + (width - 1 - k)] * ORACLE_X_AT(s);"),
+    "conv_no_bias": ("double acc = bias ? bias[d] : 0.0;\n            for (int64_t k = 0; k < width; ++k) {",
+                     "double acc = 0.0;\n            for (int64_t k = 0; k < width; ++k) {"),
+    "conv_state_ignored": ("(s_c ? s_c[hist + (s)] : 0.0)", "0.0"),
+    "conv_state_newest_first": ("(s_c ? s_c[hist + (s)] : 0.0)", "(s_c ? s_c[-(s) - 1] : 0.0)"),
+    "conv_state_out_window": ("const int64_t s = seqlen - hist + j;", "const int64_t s = seqlen - width + j;"),
+    "conv_no_silu": ("u[c * seqlen + t] = silu ? oracle_silu(acc) : acc;", "u[c * seqlen + t] = acc;"),
+    "conv_step_no_shift": ("s_c[k] = s_c[k + 1];", "s_c[k] = s_c[k];"),
+    "conv_step_current_tap": ("acc += w[d * width + hist] * x[c];", "acc += w[d * width] * x[c];"),
+    "conv_step_taps_shifted": ("acc += w[d * width + k] * s_c[k];", "acc += w[d * width + k + 1] * s_c[k];"),
 }
 
 
