@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-conv", action="store_true", help="skip the convolution kernels")
     ap.add_argument("--no-other", action="store_true", help="skip the other scan workloads")
     ap.add_argument("--settle-s", type=float, default=0.5,
                     help="seconds of untimed load before the timed region (clock settling)")
@@ -89,6 +90,7 @@ TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "scan_kernel": ["scan_fwd.cu", "ssm_device.cuh", "ssm_internal.h"],
     "step_stream_kernel": ["state_update.cu", "ssm_device.cuh", "ssm_internal.h"],
+    "conv1d_stream_kernel": ["conv1d.cu", "ssm_device.cuh", "ssm_internal.h"],
 }
 
 
@@ -494,6 +496,72 @@ def run_ours(args):
                          "l2": "L2 flushed before every token (256 MB written, then another 256 MB read "
                                "so the written lines are back in HBM); state 83.9 MB"}
         out["gpu_launches"] += wd.seqlen + 4
+
+    # ---- the short convolution in front of the scan: the layer shape (sequence
+    # form) and the decode batch (one token), L2 flushed before every launch
+    if not args.no_conv:
+        from mamba_selective_scan_02_b300.inputs import make_conv_inputs
+        from mamba_selective_scan_02_b300.roofline import algorithmic_bytes_conv, algorithmic_bytes_conv_step
+        cw = 4
+        ci = make_conv_inputs(w.batch, w.dim, w.seqlen, cw, w.io_dtype, seed=31, device=dev)
+        cu = torch.empty_like(ci["x"])
+        cso = torch.empty_like(ci["state"])
+        cp = api.conv_params(ci["x"], ci["weight"], ci["bias"], ci["state"], u=cu, state_out=cso)
+        for _ in range(3):
+            capi.check(capi.ssm_conv1d_fwd(cp, sh), "ssm_conv1d_fwd")
+        tms = []
+        for _ in range(50):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            capi.ssm_conv1d_fwd(cp, sh)
+            e1.record(stream)
+            tms.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        cms = statistics.median(a_.elapsed_time(b_) for a_, b_ in tms)
+        cbytes = algorithmic_bytes_conv(w.batch, w.dim, w.seqlen, cw, ci["x"].element_size())
+        cgbs = cbytes / (cms / 1e3) / 1e9
+        conv = {"workload": f"conv1d_W{cw}_b{w.batch}_D{w.dim}_L{w.seqlen}", "ms": cms,
+                "value": w.batch * w.dim * w.seqlen / (cms / 1e3) / 1e9, "unit": UNIT,
+                "roofline": {"bound": "hbm", "achieved": cgbs, "peak": hbm_peak, "unit": "GB/s",
+                             "frac": cgbs / hbm_peak, "traffic": recorded_traffic("conv1d_stream_kernel"),
+                             "algorithmic_bytes": cbytes},
+                "l2": "L2 flushed before every launch (256 MB written, 256 MB read)"}
+        del ci, cu, cso
+        wd = WORKLOADS[DECODE]
+        si = make_conv_inputs(wd.batch, wd.dim, 8, cw, wd.io_dtype, seed=32, device=dev, decode=True)
+        sstate = si["state"].clone()
+        su = torch.empty((wd.batch, wd.dim), dtype=si["x"].dtype, device=dev)
+        sp = []
+        for t in range(8):
+            q = capi.ConvStepParams()
+            q.batch, q.dim, q.width = wd.batch, wd.dim, cw
+            q.io_dtype = capi.SSM_BF16 if si["x"].dtype == torch.bfloat16 else capi.SSM_F32
+            q.state, q.x, q.weight, q.bias = (sstate.data_ptr(), si["x"][t].data_ptr(),
+                                              si["weight"].data_ptr(), si["bias"].data_ptr())
+            q.silu, q.u = 1, su.data_ptr()
+            sp.append(q)
+        for t in range(3):
+            capi.check(capi.ssm_conv1d_step(sp[t], sh), "ssm_conv1d_step")
+        tms = []
+        for t in range(8):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            capi.ssm_conv1d_step(sp[t], sh)
+            e1.record(stream)
+            tms.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        sms = statistics.median(a_.elapsed_time(b_) for a_, b_ in tms)
+        sbytes = algorithmic_bytes_conv_step(wd.batch, wd.dim, cw, si["x"].element_size())
+        sgbs = sbytes / (sms / 1e3) / 1e9
+        conv["decode_step"] = {"workload": f"conv1d_step_W{cw}_b{wd.batch}_D{wd.dim}", "ms": sms,
+                               "roofline": {"bound": "hbm", "achieved": sgbs, "peak": hbm_peak,
+                                            "unit": "GB/s", "frac": sgbs / hbm_peak,
+                                            "algorithmic_bytes": sbytes}}
+        out["conv1d"] = conv
+        out["gpu_launches"] += 53 + 11
+        del si, sstate, su
 
     # ---- CPU baseline: the fp64 oracle on a bounded sample (rank 0 only)
     if rank == 0 and not args.no_cpu_baseline:

@@ -130,6 +130,74 @@ typedef struct {
 /* One decode token for every (b, d): the recurrence with L = 1 on `state`. */
 ssm_status ssm_state_update(const ssm_step_params *p, ssm_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * The short convolution in front of the SSM.
+ *
+ * Operation, per batch b, channel d and token t (W = width):
+ *
+ *   u[b,d,t] = silu(bias[d] + Σ_{k=0}^{W−1} weight[d,k] · x[b,d,t−(W−1)+k])
+ *              (or without the silu when silu = 0)
+ *
+ * where x at a time before the sequence is read from state_in (the W−1 inputs
+ * just before x[b,d,0], oldest first; zeros if NULL).  The taps are in time
+ * order: weight[d,W−1] multiplies the current input.  state_out receives the
+ * last W−1 inputs of the sequence, oldest first, reaching into state_in when
+ * L < W−1, so that a later call on the continuation carries on exactly.
+ *
+ * Source: a causal depthwise convolution of width 4 followed by SiLU feeds the
+ * SSM branch of the block ("Mamba and selective state spaces, from first
+ * principles", "The Mamba block"; the erikxu.me notes, "Mamba Architecture");
+ * its three carried inputs per channel are part of the decode state (same
+ * first-principles page, "A fixed state against a growing cache").  Its output
+ * u is the scan's input u and the input of the projections that form Δ, B and
+ * C, so it is written to memory rather than fused into the scan.
+ *
+ * Pointers are device pointers, aligned to their element size (4 bytes for the
+ * fp32 weight and bias); 16-byte aligned x and u with L a multiple of 8 take
+ * the vectorised path, anything else a slower scalar one.  u must not overlap
+ * x; state_out must not overlap x, u or state_in.
+ * ------------------------------------------------------------------------ */
+
+/* Largest convolution width the kernels are built for. */
+#define SSM_MAX_CONV_WIDTH 4
+
+typedef struct {
+    int64_t batch;          /* b >= 1 */
+    int64_t dim;            /* D >= 1 (channels) */
+    int64_t seqlen;         /* L >= 1 */
+    int64_t width;          /* W in [1, SSM_MAX_CONV_WIDTH] (the block uses 4) */
+    ssm_dtype io_dtype;     /* dtype of x, u, state_in and state_out */
+    const void *x;          /* b × D × L: the convolution's input */
+    const float *weight;    /* D × W fp32, taps oldest first */
+    const float *bias;      /* D fp32; NULL = 0 */
+    int silu;               /* 1: apply SiLU; 0: plain convolution + bias */
+    const void *state_in;   /* b × D × (W−1); NULL = zeros (ignored when W = 1) */
+    void *u;                /* out: b × D × L */
+    void *state_out;        /* out: b × D × (W−1); NULL = not written */
+} ssm_conv_params;
+
+/* Causal depthwise convolution (+ bias, + SiLU) over whole sequences. */
+ssm_status ssm_conv1d_fwd(const ssm_conv_params *p, ssm_stream_t stream);
+
+typedef struct {
+    int64_t batch;          /* b >= 1 */
+    int64_t dim;            /* D >= 1 */
+    int64_t width;          /* W in [1, SSM_MAX_CONV_WIDTH] */
+    ssm_dtype io_dtype;     /* dtype of state, x and u */
+    void *state;            /* b × D × (W−1): the last W−1 inputs, oldest first; read,
+                               then shifted by one input in place (may be NULL when W = 1) */
+    const void *x;          /* b × D: this token's input */
+    const float *weight;    /* D × W fp32 */
+    const float *bias;      /* D fp32; NULL = 0 */
+    int silu;
+    void *u;                /* out: b × D */
+} ssm_conv_step_params;
+
+/* One decode token of the convolution: u from the carried inputs and x, then
+ * the state drops its oldest input and appends x.  u must not overlap x or
+ * the state. */
+ssm_status ssm_conv1d_step(const ssm_conv_step_params *p, ssm_stream_t stream);
+
 /* Size of the scratch array that ssm_scan_fwd_noalloc keeps inside the
  * library (16 MiB, held on every GPU that loads the library until exit). */
 #define SSM_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -143,6 +143,72 @@ def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, *,
     return y
 
 
+def conv_params(x, weight, bias=None, state_in=None, *, u, state_out=None, silu=True) -> capi.ConvParams:
+    """Validate tensors and build the convolution's C parameter struct."""
+    if x.dtype not in _DT:
+        raise ValueError(f"unsupported I/O dtype {x.dtype}")
+    dev = x.device
+    b, dim, L = x.shape
+    W = weight.shape[1]
+    io = x.dtype
+    _need(x, "x", (b, dim, L), io, dev)
+    _need(weight, "weight", (dim, W), torch.float32, dev)
+    _opt(bias, "bias", (dim,), torch.float32, dev)
+    _opt(state_in, "state_in", (b, dim, W - 1), io, dev)
+    _need(u, "u", (b, dim, L), io, dev)
+    _opt(state_out, "state_out", (b, dim, W - 1), io, dev)
+    p = capi.ConvParams()
+    p.batch, p.dim, p.seqlen, p.width = b, dim, L, W
+    p.io_dtype = _DT[io]
+    p.x, p.weight, p.bias = _ptr(x), _ptr(weight), _ptr(bias)
+    p.silu = int(bool(silu))
+    p.state_in, p.u, p.state_out = _ptr(state_in), _ptr(u), _ptr(state_out)
+    return p
+
+
+def conv1d(x, weight, bias=None, state_in=None, *, silu=True, u=None, state_out=None,
+           return_state=True, stream=None):
+    """Causal depthwise convolution (+ bias, + SiLU) of x (b, D, L) with weight
+    (D, W).  Returns (u, state_out); state_out (b, D, W-1) holds the last W-1
+    inputs (None if not requested)."""
+    if u is None:
+        u = torch.empty_like(x)
+    if state_out is None and return_state:
+        state_out = torch.empty((x.shape[0], x.shape[1], weight.shape[1] - 1), dtype=x.dtype, device=x.device)
+    p = conv_params(x, weight, bias, state_in, u=u, state_out=state_out, silu=silu)
+    st = torch.cuda.current_stream(x.device).cuda_stream if stream is None else stream
+    capi.check(capi.ssm_conv1d_fwd(p, st), "ssm_conv1d_fwd")
+    return u, state_out
+
+
+def conv1d_step(state, x, weight, bias=None, *, silu=True, u=None, stream=None):
+    """One decode token of the convolution: x (b, D); ``state`` (b, D, W-1) is
+    shifted in place.  Returns u (b, D)."""
+    if x.dtype not in _DT:
+        raise ValueError(f"unsupported I/O dtype {x.dtype}")
+    dev = x.device
+    b, dim = x.shape
+    W = weight.shape[1]
+    if u is None:
+        u = torch.empty_like(x)
+    _need(x, "x", (b, dim), x.dtype, dev)
+    _need(weight, "weight", (dim, W), torch.float32, dev)
+    _opt(bias, "bias", (dim,), torch.float32, dev)
+    if W > 1:
+        _need(state, "state", (b, dim, W - 1), x.dtype, dev)
+    _need(u, "u", (b, dim), x.dtype, dev)
+    p = capi.ConvStepParams()
+    p.batch, p.dim, p.width = b, dim, W
+    p.io_dtype = _DT[x.dtype]
+    p.state = _ptr(state) if W > 1 else None
+    p.x, p.weight, p.bias = _ptr(x), _ptr(weight), _ptr(bias)
+    p.silu = int(bool(silu))
+    p.u = _ptr(u)
+    st = torch.cuda.current_stream(dev).cuda_stream if stream is None else stream
+    capi.check(capi.ssm_conv1d_step(p, st), "ssm_conv1d_step")
+    return u
+
+
 def workspace_status(workspace, stream=None) -> int:
     """Synchronise and return the device status recorded in a scan workspace."""
     st = torch.cuda.current_stream(workspace.device).cuda_stream if stream is None else stream

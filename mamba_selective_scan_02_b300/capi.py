@@ -16,6 +16,7 @@ from . import build as _build
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT = range(5)
 SSM_F32, SSM_BF16 = 0, 1
 SSM_MAX_DSTATE = 16
+SSM_MAX_CONV_WIDTH = 4
 SSM_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _vp = ctypes.c_void_p
@@ -43,6 +44,24 @@ class StepParams(ctypes.Structure):
         ("A", _vp), ("Dskip", _vp), ("delta_bias", _vp),
         ("delta_softplus", ctypes.c_int), ("zoh", ctypes.c_int),
         ("y", _vp),
+    ]
+
+
+class ConvParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("seqlen", _i64), ("width", _i64),
+        ("io_dtype", ctypes.c_int),
+        ("x", _vp), ("weight", _vp), ("bias", _vp), ("silu", ctypes.c_int),
+        ("state_in", _vp), ("u", _vp), ("state_out", _vp),
+    ]
+
+
+class ConvStepParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("width", _i64),
+        ("io_dtype", ctypes.c_int),
+        ("state", _vp), ("x", _vp), ("weight", _vp), ("bias", _vp), ("silu", ctypes.c_int),
+        ("u", _vp),
     ]
 
 
@@ -77,6 +96,10 @@ def lib():
             L.ssm_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ScanParams), _vp]
             L.ssm_state_update.restype = ctypes.c_int
             L.ssm_state_update.argtypes = [ctypes.POINTER(StepParams), _vp]
+            L.ssm_conv1d_fwd.restype = ctypes.c_int
+            L.ssm_conv1d_fwd.argtypes = [ctypes.POINTER(ConvParams), _vp]
+            L.ssm_conv1d_step.restype = ctypes.c_int
+            L.ssm_conv1d_step.argtypes = [ctypes.POINTER(ConvStepParams), _vp]
             L.ssm_workspace_status.restype = ctypes.c_int
             L.ssm_workspace_status.argtypes = [_vp, _vp]
             L.ssm_status_string.restype = ctypes.c_char_p
@@ -125,6 +148,14 @@ def ssm_scan_fwd_noalloc(p: ScanParams, stream: int) -> int:
 
 def ssm_state_update(p: StepParams, stream: int) -> int:
     return lib().ssm_state_update(ctypes.byref(p), stream)
+
+
+def ssm_conv1d_fwd(p: ConvParams, stream: int) -> int:
+    return lib().ssm_conv1d_fwd(ctypes.byref(p), stream)
+
+
+def ssm_conv1d_step(p: ConvStepParams, stream: int) -> int:
+    return lib().ssm_conv1d_step(ctypes.byref(p), stream)
 
 
 def ssm_workspace_status(workspace: int, stream: int) -> int:

@@ -188,6 +188,77 @@ ssm_status ssm_state_update(const ssm_step_params *p, ssm_stream_t stream) {
                : SSM_ERR_CUDA;
 }
 
+ssm_status ssm_conv1d_fwd(const ssm_conv_params *p, ssm_stream_t stream) {
+    if (!p) return SSM_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->dim < 1 || p->seqlen < 1) return SSM_ERR_INVALID_ARG;
+    if (p->width < 1) return SSM_ERR_INVALID_ARG;
+    if (p->width > SSM_MAX_CONV_WIDTH) return SSM_ERR_UNSUPPORTED;
+    if (p->io_dtype != SSM_F32 && p->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (p->silu != 0 && p->silu != 1) return SSM_ERR_INVALID_ARG;
+    if (!p->x || !p->weight || !p->u) return SSM_ERR_INVALID_ARG;
+    if (p->batch > (int64_t(1) << 40) / p->dim || p->batch * p->dim > (int64_t(1) << 40) / p->seqlen)
+        return SSM_ERR_UNSUPPORTED;
+    const size_t es = p->io_dtype == SSM_BF16 ? 2 : 4;
+    const void *aio[] = {p->x, p->u, p->state_in, p->state_out};
+    for (const void *q : aio)
+        if (q && (reinterpret_cast<uintptr_t>(q) % es) != 0) return SSM_ERR_INVALID_ARG;
+    if (!aligned4(p->weight) || (p->bias && !aligned4(p->bias))) return SSM_ERR_INVALID_ARG;
+    const size_t seq = (size_t)p->batch * p->dim * p->seqlen * es;
+    const size_t st = (size_t)p->batch * p->dim * (p->width - 1) * es;
+    if (overlaps(p->u, seq, p->x, seq)) return SSM_ERR_INVALID_ARG;
+    if (st > 0 && (overlaps(p->state_out, st, p->state_in, st) || overlaps(p->state_out, st, p->x, seq) ||
+                   overlaps(p->state_out, st, p->u, seq)))
+        return SSM_ERR_INVALID_ARG;
+    ssm::ConvArgs a;
+    a.batch = p->batch;
+    a.dim = p->dim;
+    a.seqlen = p->seqlen;
+    a.width = (int)p->width;
+    a.x = p->x;
+    a.w = p->weight;
+    a.bias = p->bias;
+    a.state_in = p->width > 1 ? p->state_in : nullptr;
+    a.u = p->u;
+    a.state_out = p->width > 1 ? p->state_out : nullptr;
+    a.silu = p->silu;
+    return ssm::conv_launch(a, p->io_dtype == SSM_BF16, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SSM_OK
+               : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_conv1d_step(const ssm_conv_step_params *p, ssm_stream_t stream) {
+    if (!p) return SSM_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->dim < 1 || p->width < 1) return SSM_ERR_INVALID_ARG;
+    if (p->width > SSM_MAX_CONV_WIDTH) return SSM_ERR_UNSUPPORTED;
+    if (p->io_dtype != SSM_F32 && p->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (p->silu != 0 && p->silu != 1) return SSM_ERR_INVALID_ARG;
+    if (!p->x || !p->weight || !p->u || (p->width > 1 && !p->state)) return SSM_ERR_INVALID_ARG;
+    if (p->batch > (int64_t(1) << 40) / p->dim) return SSM_ERR_UNSUPPORTED;
+    const size_t es = p->io_dtype == SSM_BF16 ? 2 : 4;
+    const void *aio[] = {p->x, p->u, p->state};
+    for (const void *q : aio)
+        if (q && (reinterpret_cast<uintptr_t>(q) % es) != 0) return SSM_ERR_INVALID_ARG;
+    if (!aligned4(p->weight) || (p->bias && !aligned4(p->bias))) return SSM_ERR_INVALID_ARG;
+    const size_t nch = (size_t)p->batch * p->dim;
+    const size_t st = nch * (p->width - 1) * es;
+    if (overlaps(p->u, nch * es, p->x, nch * es) || (st > 0 && overlaps(p->u, nch * es, p->state, st)))
+        return SSM_ERR_INVALID_ARG;
+    ssm::ConvStepArgs a;
+    a.batch = p->batch;
+    a.dim = p->dim;
+    a.width = (int)p->width;
+    a.state = p->width > 1 ? p->state : nullptr;
+    a.x = p->x;
+    a.w = p->weight;
+    a.bias = p->bias;
+    a.u = p->u;
+    a.silu = p->silu;
+    return ssm::conv_step_launch(a, p->io_dtype == SSM_BF16, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? SSM_OK
+               : SSM_ERR_CUDA;
+}
+
 ssm_status ssm_workspace_status(const void *workspace, ssm_stream_t stream) {
     if (!workspace) return SSM_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

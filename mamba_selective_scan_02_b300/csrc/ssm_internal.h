@@ -53,10 +53,36 @@ struct StepArgs {
     void *y;
 };
 
+// Causal depthwise convolution + bias + optional SiLU over whole sequences.
+struct ConvArgs {
+    int64_t batch, dim, seqlen;
+    int width;               // W in [1, 4]
+    const void *x;           // b × D × L
+    const float *w;          // D × W, taps oldest first
+    const float *bias;       // D or nullptr
+    const void *state_in;    // b × D × (W-1) or nullptr
+    void *u;                 // b × D × L
+    void *state_out;         // b × D × (W-1) or nullptr
+    int silu;
+};
+
+// One decode token of the convolution; the state shifts in place.
+struct ConvStepArgs {
+    int64_t batch, dim;
+    int width;
+    void *state;             // b × D × (W-1)
+    const void *x;           // b × D
+    const float *w, *bias;
+    void *u;                 // b × D
+    int silu;
+};
+
 int scan_groups(int64_t dstate);
 ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t requested);
 cudaError_t scan_launch(const ScanArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t step_launch(const StepArgs &a, bool bf16, cudaStream_t stream);
+cudaError_t conv_launch(const ConvArgs &a, bool bf16, cudaStream_t stream);
+cudaError_t conv_step_launch(const ConvStepArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t mufu_ex2_launch(float *sink, int blocks, int iters, cudaStream_t stream);
 
 }  // namespace ssm

@@ -124,4 +124,28 @@ def make_inputs(w: Workload | str, device="cpu", batch: int | None = None,
                 seqlen=L)
 
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "s4d_real_A", "torch_dtype"]
+def make_conv_inputs(batch: int, dim: int, seqlen: int, width: int = 4, io_dtype: str = "bf16",
+                     seed: int = 0, device="cpu", with_state: bool = True, decode: bool = False) -> dict:
+    """Seeded inputs for the short convolution in front of the scan.
+
+    x ~ N(0, 1) in the I/O dtype (the input projection's output); weight and
+    bias ~ U(-1/sqrt(W), 1/sqrt(W)) in fp32, the default initialisation of a
+    depthwise convolution whose fan-in is its width; the carried state (the
+    W-1 inputs before the sequence) ~ N(0, 1) in the I/O dtype, or None.
+    x is (b, D, L), or (T, b, D) for ``decode`` (T = seqlen consecutive tokens).
+    Draw order: x, weight, bias, state."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = torch_dtype(io_dtype)
+    shape = (seqlen, batch, dim) if decode else (batch, dim, seqlen)
+    x = torch.randn(shape, generator=g, dtype=torch.float32, device=device).to(dt)
+    bound = 1.0 / (width ** 0.5)
+    weight = (torch.rand((dim, width), generator=g, dtype=torch.float32, device=device) * 2 - 1) * bound
+    bias = (torch.rand(dim, generator=g, dtype=torch.float32, device=device) * 2 - 1) * bound
+    state = None
+    if with_state:
+        state = torch.randn((batch, dim, width - 1), generator=g, dtype=torch.float32, device=device).to(dt)
+    return dict(x=x, weight=weight, bias=bias, state=state)
+
+
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "make_conv_inputs", "s4d_real_A", "torch_dtype"]

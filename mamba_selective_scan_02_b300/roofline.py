@@ -31,6 +31,23 @@ def algorithmic_bytes_step(batch: int, dim: int, dstate: int, io_bytes: int,
     return n
 
 
+def algorithmic_bytes_conv(batch: int, dim: int, seqlen: int, width: int, io_bytes: int,
+                           has_state_in: bool = True, has_state_out: bool = True) -> int:
+    """Bytes the short convolution must move: x read and u written once per
+    (b, d, t), the W taps and the bias once per channel, the W-1 carried
+    inputs read and written once per (b, d)."""
+    n = 2 * batch * dim * seqlen * io_bytes
+    n += dim * (width + 1) * 4
+    n += batch * dim * (width - 1) * io_bytes * (int(has_state_in) + int(has_state_out))
+    return n
+
+
+def algorithmic_bytes_conv_step(batch: int, dim: int, width: int, io_bytes: int) -> int:
+    """Bytes per decode token of the convolution: the W-1 carried inputs read
+    and written, x read and u written per (b, d), taps and bias once."""
+    return batch * dim * (2 * (width - 1) + 2) * io_bytes + dim * (width + 1) * 4
+
+
 def exps_scan(batch: int, dim: int, dstate: int, seqlen: int) -> int:
     """One exponential Ā = exp(Δ·A) per (b, d, n, t)."""
     return batch * dim * dstate * seqlen

@@ -168,3 +168,67 @@ def test_misc_rejections():
     assert lib.ssm_workspace_status(None, None) == capi.SSM_ERR_INVALID_ARG
     assert lib.ssm_bench_mufu_ex2(None, 1, 1, None) == capi.SSM_ERR_INVALID_ARG
     assert lib.ssm_bench_mufu_ex2(ctypes.c_void_p(FAKE), 0, 1, None) == capi.SSM_ERR_INVALID_ARG
+
+
+def valid_conv(**over):
+    p = capi.ConvParams()
+    p.batch, p.dim, p.seqlen, p.width = 2, 64, 256, 4
+    p.io_dtype = capi.SSM_BF16
+    step = 1 << 20
+    p.x, p.weight, p.bias = FAKE, FAKE + step, FAKE + 2 * step
+    p.silu = 1
+    p.state_in, p.u, p.state_out = FAKE + 3 * step, FAKE + 4 * step, FAKE + 5 * step
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(batch=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(seqlen=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(width=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(width=5), capi.SSM_ERR_UNSUPPORTED),
+    (dict(io_dtype=9), capi.SSM_ERR_INVALID_ARG),
+    (dict(silu=3), capi.SSM_ERR_INVALID_ARG),
+    (dict(x=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(weight=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(u=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(x=FAKE + 1), capi.SSM_ERR_INVALID_ARG),                     # bf16 at an odd address
+    (dict(weight=FAKE + (1 << 20) + 2), capi.SSM_ERR_INVALID_ARG),    # fp32 weight not 4-byte aligned
+    (dict(u=FAKE + 512), capi.SSM_ERR_INVALID_ARG),                   # u overlaps x
+    (dict(state_out=FAKE + 3 * (1 << 20) + 2), capi.SSM_ERR_INVALID_ARG),  # state_out overlaps state_in
+    (dict(state_out=FAKE + 4 * (1 << 20) + 64), capi.SSM_ERR_INVALID_ARG),  # state_out inside u
+])
+def test_conv_rejects_before_launch(over, code):
+    assert capi.ssm_conv1d_fwd(valid_conv(**over), None) == code
+
+
+def valid_conv_step(**over):
+    p = capi.ConvStepParams()
+    p.batch, p.dim, p.width = 4, 64, 4
+    p.io_dtype = capi.SSM_F32
+    step = 1 << 20
+    p.state, p.x, p.weight, p.bias, p.u = FAKE, FAKE + step, FAKE + 2 * step, FAKE + 3 * step, FAKE + 4 * step
+    p.silu = 1
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(batch=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(width=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(width=8), capi.SSM_ERR_UNSUPPORTED),
+    (dict(state=None), capi.SSM_ERR_INVALID_ARG),                     # W > 1 needs a state
+    (dict(x=FAKE + (1 << 20) + 2), capi.SSM_ERR_INVALID_ARG),         # fp32 at a 2-byte offset
+    (dict(u=FAKE + (1 << 20)), capi.SSM_ERR_INVALID_ARG),             # u is x
+    (dict(u=FAKE + 16), capi.SSM_ERR_INVALID_ARG),                    # u inside the state
+    (dict(silu=-1), capi.SSM_ERR_INVALID_ARG),
+])
+def test_conv_step_rejects_before_launch(over, code):
+    assert capi.ssm_conv1d_step(valid_conv_step(**over), None) == code
+
+
+def test_conv_null_params():
+    assert capi.lib().ssm_conv1d_fwd(None, None) == capi.SSM_ERR_INVALID_ARG
+    assert capi.lib().ssm_conv1d_step(None, None) == capi.SSM_ERR_INVALID_ARG
