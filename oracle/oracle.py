@@ -56,6 +56,11 @@ def _bind(lib):
     lib.oracle_conv1d.argtypes = [_I64, _I64, _I64, _I64, _D, _D, _D, ctypes.c_int, _D, _D, _D]
     lib.oracle_conv1d_step.restype = ctypes.c_int
     lib.oracle_conv1d_step.argtypes = [_I64, _I64, _I64, _D, _D, _D, _D, ctypes.c_int, _D]
+    lib.oracle_scan_bwd.restype = ctypes.c_int
+    lib.oracle_scan_bwd.argtypes = [_I64, _I64, _I64, _I64,
+                                    _D, _D, _D, _D, _D, _D, _D, _D,
+                                    ctypes.c_int, ctypes.c_int, _D, _D, _D,
+                                    _D, _D, _D, _D, _D, _D, _D, _D, _D, _I64, _I64]
     lib.oracle_step.restype = ctypes.c_int
     lib.oracle_step.argtypes = [_I64, _I64, _I64,
                                 _D, _D, _D, _D, _D, _D, _D, _D, _D,
@@ -179,3 +184,47 @@ def conv1d_step(state, x, w, bias=None, silu=True, lib=None):
     if rc != 0:
         raise RuntimeError("oracle_conv1d_step failed")
     return u, st
+
+
+def scan_bwd(u, delta, A, B, C, dy, Dskip=None, z=None, bias=None, h0=None, dhL=None,
+             delta_softplus=True, zoh=False, threads: int = 1, lib=None):
+    """Gradient of the forward scan for upstream gradients dy (b, D, L) and dhL
+    (b, D, N) or None.  Returns a dict of fp64 arrays: du, ddelta, dz (None
+    without z), dB, dC, dA, dDskip, dbias, dh0 (None without h0).
+
+    ``threads`` > 1 splits the (b, d) channels over host threads; each range
+    adds into its own dB, dC, dA, dDskip, dbias buffers, summed at the end."""
+    lib = lib or load()
+    u, delta, z, B, C, A, Dskip, bias, h0, dy, dhL = map(
+        _f64, (u, delta, z, B, C, A, Dskip, bias, h0, dy, dhL))
+    b, dim, L = u.shape
+    N = A.shape[1]
+    assert dy.shape == u.shape and B.shape == (b, N, L) and C.shape == (b, N, L)
+    du = np.empty((b, dim, L))
+    ddelta = np.empty((b, dim, L))
+    dz = np.empty((b, dim, L)) if z is not None else None
+    dh0 = np.empty((b, dim, N)) if h0 is not None else None
+    nch = b * dim
+    bounds = np.linspace(0, nch, max(1, min(threads, nch)) + 1).astype(np.int64)
+    parts = []
+
+    def run(i):
+        acc = dict(dB=np.zeros((b, N, L)), dC=np.zeros((b, N, L)), dA=np.zeros((dim, N)),
+                   dDskip=np.zeros(dim), dbias=np.zeros(dim))
+        rc = lib.oracle_scan_bwd(b, dim, N, L, _p(u), _p(delta), _p(z), _p(B), _p(C), _p(A),
+                                 _p(Dskip), _p(bias), int(bool(delta_softplus)), int(bool(zoh)),
+                                 _p(h0), _p(dy), _p(dhL), _p(du), _p(ddelta), _p(dz),
+                                 _p(acc["dB"]), _p(acc["dC"]), _p(acc["dA"]), _p(acc["dDskip"]),
+                                 _p(acc["dbias"]), _p(dh0), int(bounds[i]), int(bounds[i + 1]))
+        if rc != 0:
+            raise RuntimeError("oracle_scan_bwd failed")
+        return acc
+
+    if len(bounds) == 2:
+        parts = [run(0)]
+    else:
+        with ThreadPoolExecutor(len(bounds) - 1) as ex:
+            parts = list(ex.map(run, range(len(bounds) - 1)))
+    out = {k: sum(p[k] for p in parts) for k in parts[0]}
+    out.update(du=du, ddelta=ddelta, dz=dz, dh0=dh0)
+    return out

@@ -55,6 +55,17 @@
  * filter in time order, oldest first); SiLU is optional so the plain
  * convolution can be checked on its own.
  *
+ * The backward scan (oracle_scan_bwd) is the gradient of that forward map for
+ * a loss whose gradient with respect to y is dy and with respect to hL is dhL
+ * [the training half of the hardware-aware scan: erikxu.me notes — "GPU Memory
+ * Hierarchy"; first-principles page — "The hardware-aware scan", which
+ * recomputes the intermediate states in the backward pass instead of storing
+ * them].  It runs the adjoint of the recurrence backwards in time,
+ *   λ_t = C_t ŷ_t + Ā_{t+1} λ_{t+1},  λ_L = dhL,  ŷ_t = dy_t · silu(z_t),
+ * and reads every input's gradient off it by the chain rule; the pages give no
+ * formulas, so this is calculus on the forward definition above, and it is
+ * pinned to central finite differences of oracle_scan.
+ *
  * Parity is pinned by tests/test_oracle_pins.py (worked example, convolution
  * kernel, gated-RNN reduction, Δ limits, first output, product-form brute
  * force, continuation; for the short convolution: numpy's convolution, the
@@ -265,5 +276,137 @@ int oracle_conv1d_step(int64_t batch, int64_t dim, int64_t width, double *state,
         if (hist > 0)
             s_c[hist - 1] = x[c];
     }
+    return 0;
+}
+
+/*
+ * Gradient of the forward scan over channels [channel_begin, channel_end).
+ * Inputs are those of oracle_scan, plus
+ *   dy  : batch × dim × seqlen, ∂loss/∂y
+ *   dhL : batch × dim × dstate, ∂loss/∂hL; NULL = 0
+ * Written for the channels in range (any may be NULL = not wanted):
+ *   du, ddelta (∂loss/∂Δraw), dz : batch × dim × seqlen
+ *   dh0                          : batch × dim × dstate
+ * ADDED to (the caller zeroes them; each channel range may use its own
+ * buffers, to be summed afterwards):
+ *   dB, dC : batch × dstate × seqlen   (sums over the channels)
+ *   dA     : dim × dstate             (sums over batch and time)
+ *   dDskip, dbias : dim
+ * Returns 0, or -1 if dstate < 1 or scratch cannot be allocated.
+ */
+int oracle_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                    const double *u, const double *delta, const double *z,
+                    const double *B, const double *C, const double *A,
+                    const double *Dskip, const double *bias,
+                    int delta_softplus, int zoh, const double *h0,
+                    const double *dy, const double *dhL,
+                    double *du, double *ddelta, double *dz, double *dB, double *dC,
+                    double *dA, double *dDskip, double *dbias, double *dh0,
+                    int64_t channel_begin, int64_t channel_end)
+{
+    if (dstate < 1)
+        return -1;
+    const int64_t N = dstate, L = seqlen;
+    /* h[(t + 1) * N + n] = h_t,n for t = -1 .. L-1; dt[t] = Δ_t; pre[t] = C·h + D·u */
+    double *h = (double *)malloc((size_t)(L + 1) * N * sizeof(double));
+    double *dt = (double *)malloc((size_t)L * sizeof(double));
+    double *pre = (double *)malloc((size_t)L * sizeof(double));
+    double *lam = (double *)malloc((size_t)N * sizeof(double));
+    if (!h || !dt || !pre || !lam) {
+        free(h); free(dt); free(pre); free(lam);
+        return -1;
+    }
+    if (channel_end > batch * dim)
+        channel_end = batch * dim;
+
+    for (int64_t c = channel_begin; c < channel_end; ++c) {
+        const int64_t b = c / dim;
+        const int64_t d = c % dim;
+        const double *u_c = u + c * L;
+        const double *dr_c = delta + c * L;
+        const double *z_c = z ? z + c * L : NULL;
+        const double *dy_c = dy + c * L;
+        const double *B_b = B + b * N * L;
+        const double *C_b = C + b * N * L;
+        const double *A_d = A + d * N;
+        const double skip = Dskip ? Dskip[d] : 0.0;
+        const double bias_d = bias ? bias[d] : 0.0;
+
+        /* forward, keeping every state */
+        for (int64_t n = 0; n < N; ++n)
+            h[n] = h0 ? h0[c * N + n] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            double x = dr_c[t] + bias_d;
+            dt[t] = delta_softplus ? oracle_softplus(x) : x;
+            double s = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double abar = exp(dt[t] * A_d[n]);
+                const double bbar = oracle_bbar(dt[t], A_d[n], B_b[n * L + t], zoh);
+                h[(t + 1) * N + n] = abar * h[t * N + n] + bbar * u_c[t];
+                s += C_b[n * L + t] * h[(t + 1) * N + n];
+            }
+            pre[t] = s + skip * u_c[t];
+        }
+
+        /* backward in time */
+        for (int64_t n = 0; n < N; ++n)
+            lam[n] = dhL ? dhL[c * N + n] : 0.0;
+        for (int64_t t = L - 1; t >= 0; --t) {
+            double gate = 1.0;
+            if (z_c) {
+                const double sg = 1.0 / (1.0 + exp(-z_c[t]));
+                gate = z_c[t] * sg;
+                /* silu'(z) = σ(z) (1 + z (1 − σ(z))) */
+                if (dz)
+                    dz[c * L + t] = dy_c[t] * pre[t] * sg * (1.0 + z_c[t] * (1.0 - sg));
+            }
+            const double yhat = dy_c[t] * gate;          /* ∂loss/∂(C·h + D·u) */
+            double du_t = yhat * skip;
+            double ddt = 0.0;
+            if (dDskip)
+                dDskip[d] += yhat * u_c[t];
+            for (int64_t n = 0; n < N; ++n) {
+                const double a = A_d[n];
+                const double Bv = B_b[n * L + t];
+                const double hprev = h[t * N + n];
+                const double abar = exp(dt[t] * a);
+                lam[n] += C_b[n * L + t] * yhat;         /* λ_t: readout at t joins */
+                dC[b * N * L + n * L + t] += yhat * h[(t + 1) * N + n];
+                /* h_t = Ā h_{t-1} + B̄ u_t */
+                const double dabar = lam[n] * hprev;
+                const double dbbar = lam[n] * u_c[t];
+                du_t += lam[n] * oracle_bbar(dt[t], a, Bv, zoh);
+                ddt += dabar * abar * a;                 /* ∂Ā/∂Δ = A Ā */
+                dA[d * N + n] += dabar * abar * dt[t];   /* ∂Ā/∂A = Δ Ā */
+                if (!zoh || a == 0.0) {
+                    /* B̄ = Δ B (also the A → 0 limit of the exact hold) */
+                    ddt += dbbar * Bv;
+                    dB[b * N * L + n * L + t] += dbbar * dt[t];
+                    if (zoh)                             /* ∂B̄/∂A at A = 0: Δ² B / 2 */
+                        dA[d * N + n] += dbbar * Bv * dt[t] * dt[t] * 0.5;
+                } else {
+                    /* B̄ = (Ā − 1)/A · B */
+                    ddt += dbbar * abar * Bv;                               /* ∂B̄/∂Δ = Ā B */
+                    dB[b * N * L + n * L + t] += dbbar * expm1(dt[t] * a) / a;
+                    dA[d * N + n] += dbbar * Bv * (dt[t] * abar * a - expm1(dt[t] * a)) / (a * a);
+                }
+                lam[n] *= abar;                          /* on to ∂loss/∂h_{t-1} */
+            }
+            if (du)
+                du[c * L + t] = du_t;
+            /* Δ = softplus(Δraw + bias): ∂Δ/∂Δraw = σ(Δraw + bias) */
+            double dx = ddt;
+            if (delta_softplus)
+                dx *= 1.0 / (1.0 + exp(-(dr_c[t] + bias_d)));
+            if (ddelta)
+                ddelta[c * L + t] = dx;
+            if (dbias)
+                dbias[d] += dx;
+        }
+        if (dh0)
+            for (int64_t n = 0; n < N; ++n)
+                dh0[c * N + n] = lam[n];
+    }
+    free(h); free(dt); free(pre); free(lam);
     return 0;
 }

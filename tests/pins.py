@@ -409,6 +409,67 @@ def pin_block_counts(lib):
     assert g["pythia_tokens"] * 2 * g["pythia_layers"] * dm == g["whole_state"]
 
 
+# --------------------------------------------------------------------------
+# P12: the backward scan is the gradient of the forward map.  For the loss
+# Σ w_y·y + Σ w_h·hL its output must equal central finite differences of the
+# forward oracle in every input coordinate (the forward is independent code:
+# oracle_scan), with and without SiLU gate, softplus, initial state, exact
+# hold, and with an A entry of zero (the exact hold's A → 0 limit).
+
+def pin_backward_finite_differences(lib, seed=21):
+    rng = np.random.default_rng(seed)
+    b, dim, N, L = 2, 3, 4, 6
+    base = dict(u=rng.normal(size=(b, dim, L)), delta=rng.normal(size=(b, dim, L)),
+                z=rng.normal(size=(b, dim, L)), B=rng.normal(size=(b, N, L)),
+                C=rng.normal(size=(b, N, L)), A=-rng.uniform(0.2, 2.0, (dim, N)),
+                Dskip=rng.normal(size=dim), bias=rng.normal(size=dim),
+                h0=rng.normal(size=(b, dim, N)))
+    base["A"][1, 2] = 0.0
+    wy = rng.normal(size=(b, dim, L))
+    wh = rng.normal(size=(b, dim, N))
+    cases = [dict(zoh=False, softplus=True, gate=True, h0=True),
+             dict(zoh=True, softplus=True, gate=True, h0=True),
+             dict(zoh=False, softplus=False, gate=False, h0=False)]
+    for cs in cases:
+        inp = dict(base)
+        if not cs["gate"]:
+            inp["z"] = None
+        if not cs["h0"]:
+            inp["h0"] = None
+        if not cs["softplus"]:
+            inp["delta"] = np.abs(inp["delta"]) + 0.1        # Δ = Δraw + bias must stay usable
+            inp["bias"] = np.abs(inp["bias"])
+
+        def loss(**over):
+            a = dict(inp)
+            a.update(over)
+            y, hL = orc.scan(a["u"], a["delta"], a["A"], a["B"], a["C"], Dskip=a["Dskip"], z=a["z"],
+                             bias=a["bias"], h0=a["h0"], delta_softplus=cs["softplus"], zoh=cs["zoh"],
+                             lib=lib)
+            return float((wy * y).sum() + (wh * hL).sum())
+
+        g = orc.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], wy, Dskip=inp["Dskip"],
+                         z=inp["z"], bias=inp["bias"], h0=inp["h0"], dhL=wh,
+                         delta_softplus=cs["softplus"], zoh=cs["zoh"], lib=lib)
+        names = [("u", "du"), ("delta", "ddelta"), ("B", "dB"), ("C", "dC"), ("A", "dA"),
+                 ("Dskip", "dDskip"), ("bias", "dbias")]
+        if cs["gate"]:
+            names.append(("z", "dz"))
+        if cs["h0"]:
+            names.append(("h0", "dh0"))
+        eps = 1e-6
+        for name, key in names:
+            arr = inp[name]
+            fd = np.zeros_like(arr)
+            for idx in np.ndindex(arr.shape):
+                p_, m_ = arr.copy(), arr.copy()
+                p_[idx] += eps
+                m_[idx] -= eps
+                fd[idx] = (loss(**{name: p_}) - loss(**{name: m_})) / (2 * eps)
+            _close(g[key], fd, 0, 1e-7 * (1 + np.abs(fd).max()), f"backward {key} {cs}")
+
+
 ALL_PINS = [pin_worked_example, pin_lti_convolution, pin_gated_rnn, pin_delta_limits,
             pin_first_output, pin_product_form, pin_continuation, pin_decode_equals_scan,
-            pin_conv_library, pin_conv_impulse, pin_conv_continuation, pin_block_counts]
+            pin_conv_library, pin_conv_impulse, pin_conv_continuation, pin_block_counts,
+            pin_backward_finite_differences]

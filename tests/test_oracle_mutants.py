@@ -30,8 +30,8 @@ MUTANTS = {
     "gate_is_sigmoid": ("return x / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(-x));"),
     "h0_ignored": ("h[n] = h0 ? h0[c * dstate + n] : 0.0;", "h[n] = 0.0;"),
     "A_row_of_channel_0": ("const double *A_d = A + d * dstate;", "const double *A_d = A;"),
-    "skip_of_channel_0": ("const double skip = Dskip ? Dskip[d] : 0.0;",
-                          "const double skip = Dskip ? Dskip[0] : 0.0;"),
+    "skip_of_channel_0": ("const double *A_d = A + d * dstate;\n        const double skip = Dskip ? Dskip[d] : 0.0;",
+                          "const double *A_d = A + d * dstate;\n        const double skip = Dskip ? Dskip[0] : 0.0;"),
     "B_of_batch_0": ("const double *B_b = B + b * dstate * seqlen;", "const double *B_b = B;"),
     "gate_only_on_state_term": (
         "double out = s + skip * u_c[t];\n            if (z_c)\n                out *= oracle_silu(z_c[t]);",
@@ -50,6 +50,18 @@ MUTANTS = {
     "conv_step_no_shift": ("s_c[k] = s_c[k + 1];", "s_c[k] = s_c[k];"),
     "conv_step_current_tap": ("acc += w[d * width + hist] * x[c];", "acc += w[d * width] * x[c];"),
     "conv_step_taps_shifted": ("acc += w[d * width + k] * s_c[k];", "acc += w[d * width + k + 1] * s_c[k];"),
+    "bwd_readout_not_in_lambda": ("lam[n] += C_b[n * L + t] * yhat;", "lam[n] += 0.0;"),
+    "bwd_dA_missing_delta": ("dA[d * N + n] += dabar * abar * dt[t];", "dA[d * N + n] += dabar * abar;"),
+    "bwd_ddt_missing_A": ("ddt += dabar * abar * a;", "ddt += dabar * abar;"),
+    "bwd_softplus_grad_dropped": ("dx *= 1.0 / (1.0 + exp(-(dr_c[t] + bias_d)));", "dx *= 1.0;"),
+    "bwd_dz_missing_silu_prime": ("dy_c[t] * pre[t] * sg * (1.0 + z_c[t] * (1.0 - sg));",
+                                  "dy_c[t] * pre[t] * sg;"),
+    "bwd_dC_uses_prev_state": ("dC[b * N * L + n * L + t] += yhat * h[(t + 1) * N + n];",
+                               "dC[b * N * L + n * L + t] += yhat * h[t * N + n];"),
+    "bwd_zoh_dB_first_order": ("dB[b * N * L + n * L + t] += dbbar * expm1(dt[t] * a) / a;",
+                               "dB[b * N * L + n * L + t] += dbbar * dt[t];"),
+    "bwd_no_decay_propagation": ("lam[n] *= abar;", "lam[n] *= 1.0;"),
+    "bwd_dD_missing": ("dDskip[d] += yhat * u_c[t];", "dDskip[d] += 0.0;"),
 }
 
 
