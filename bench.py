@@ -91,6 +91,7 @@ KERNEL_SOURCES = {
     "scan_kernel": ["scan_fwd.cu", "ssm_device.cuh", "ssm_internal.h"],
     "step_stream_kernel": ["state_update.cu", "ssm_device.cuh", "ssm_internal.h"],
     "conv1d_stream_kernel": ["conv1d.cu", "ssm_device.cuh", "ssm_internal.h"],
+    "conv1d_step8_kernel": ["conv1d.cu", "ssm_device.cuh", "ssm_internal.h"],
 }
 
 
@@ -558,6 +559,7 @@ def run_ours(args):
         conv["decode_step"] = {"workload": f"conv1d_step_W{cw}_b{wd.batch}_D{wd.dim}", "ms": sms,
                                "roofline": {"bound": "hbm", "achieved": sgbs, "peak": hbm_peak,
                                             "unit": "GB/s", "frac": sgbs / hbm_peak,
+                                            "traffic": recorded_traffic("conv1d_step8_kernel"),
                                             "algorithmic_bytes": sbytes}}
         out["conv1d"] = conv
         out["gpu_launches"] += 53 + 11
