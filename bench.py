@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-conv", action="store_true", help="skip the convolution kernels")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward scan")
+    ap.add_argument("--bwd-batch", type=int, default=0,
+                    help="sequences of the layer the backward runs on (default: all of them)")
     ap.add_argument("--no-other", action="store_true", help="skip the other scan workloads")
     ap.add_argument("--settle-s", type=float, default=0.5,
                     help="seconds of untimed load before the timed region (clock settling)")
@@ -92,6 +95,7 @@ KERNEL_SOURCES = {
     "step_stream_kernel": ["state_update.cu", "ssm_device.cuh", "ssm_internal.h"],
     "conv1d_stream_kernel": ["conv1d.cu", "ssm_device.cuh", "ssm_internal.h"],
     "conv1d_step8_kernel": ["conv1d.cu", "ssm_device.cuh", "ssm_internal.h"],
+    "bwd_rev_kernel": ["scan_bwd.cu", "ssm_device.cuh", "ssm_internal.h"],
 }
 
 
@@ -497,6 +501,53 @@ def run_ours(args):
                          "l2": "L2 flushed before every token (256 MB written, then another 256 MB read "
                                "so the written lines are back in HBM); state 83.9 MB"}
         out["gpu_launches"] += wd.seqlen + 4
+
+    # ---- the backward scan on the same layer: dy drawn like y, L2 flushed
+    # before every launch (its inputs and outputs exceed L2 anyway)
+    if not args.no_bwd:
+        from mamba_selective_scan_02_b300.roofline import algorithmic_bytes_bwd
+        bb = args.bwd_batch or w.batch          # sequences of the layer the backward runs on
+        bi = {k: (inp[k][:bb] if k in ("u", "delta", "z", "B", "C") else inp[k]) for k in inp}
+        g = torch.Generator(device=dev).manual_seed(41)
+        dy = torch.randn(bi["u"].shape, generator=g, device=dev).to(bi["u"].dtype)
+        bshape = (bb, w.dstate, w.seqlen)
+        bout = dict(du=torch.empty_like(bi["u"]), ddelta=torch.empty_like(bi["u"]), dz=torch.empty_like(bi["u"]),
+                    dB=torch.empty(bshape, dtype=torch.float32, device=dev),
+                    dC=torch.empty(bshape, dtype=torch.float32, device=dev),
+                    dA=torch.empty((w.dim, w.dstate), dtype=torch.float32, device=dev),
+                    dD=torch.empty(w.dim, dtype=torch.float32, device=dev),
+                    ddelta_bias=torch.empty(w.dim, dtype=torch.float32, device=dev))
+        bws = torch.empty(api.bwd_workspace_bytes(bb, w.dim, w.dstate, w.seqlen), dtype=torch.uint8,
+                          device=dev)
+        bp = api.bwd_params(bi["u"], bi["delta"], bi["A"], bi["B"], bi["C"], dy, bi["Dskip"], bi["z"],
+                            bi["bias"], None, None, workspace=bws, **bout)
+        for _ in range(3):
+            capi.check(capi.ssm_scan_bwd(bp, sh), "ssm_scan_bwd")
+        tms = []
+        for _ in range(20):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            capi.ssm_scan_bwd(bp, sh)
+            e1.record(stream)
+            tms.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        capi.check(api.workspace_status(bws), "ssm_scan_bwd")
+        bms = statistics.median(a_.elapsed_time(b_) for a_, b_ in tms)
+        bbytes = algorithmic_bytes_bwd(bb, w.dim, w.dstate, w.seqlen, bi["u"].element_size())
+        bgbs = bbytes / (bms / 1e3) / 1e9
+        bex = exps * bb / w.batch / (bms / 1e3) / 1e9
+        out["backward"] = {
+            "workload": w.name, "ms": bms, "value": elems * bb / w.batch / (bms / 1e3) / 1e9, "unit": UNIT,
+            "roofline": {"bound": "hbm", "achieved": bgbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": bgbs / hbm_peak, "algorithmic_bytes": bbytes,
+                         "traffic": recorded_traffic("bwd_rev_kernel"),
+                         "mufu": {"achieved": bex, "peak": mufu_peak, "unit": "Gex2/s", "frac": bex / mufu_peak,
+                                  "note": "one exp per (b, d, n, t), the forward's count"}},
+            "kernels_per_call": 2, "batch": bb,
+            "l2": "L2 flushed before every launch (256 MB written, 256 MB read)"}
+        out["gpu_launches"] += 23 * 2
+        del dy, bout, bws, bi
 
     # ---- the short convolution in front of the scan: the layer shape (sequence
     # form) and the decode batch (one token), L2 flushed before every launch

@@ -131,6 +131,63 @@ typedef struct {
 ssm_status ssm_state_update(const ssm_step_params *p, ssm_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Backward scan: the gradient of ssm_scan_fwd.
+ *
+ * For upstream gradients dy = ∂loss/∂y and dhL = ∂loss/∂hL it returns
+ * ∂loss/∂ of u, Δraw, z, B, C, A, Dskip, delta_bias and h0.  The adjoint state
+ * runs backwards in time,
+ *
+ *   λ_t = C_t · ŷ_t + Ā_{t+1} ⊙ λ_{t+1},   λ_{L−1} starts from dhL,
+ *   ŷ_t = dy_t · silu(z_t)                  (dy_t without a gate),
+ *
+ * and the gradients are read off it by the chain rule: du_t = ŷ_t·D +
+ * Σ_n λ_t,n B̄_t,n; dC_t,n = Σ_d ŷ_t h_t,n; dB, dΔ, dA from ∂Ā/∂Δ = A·Ā,
+ * ∂Ā/∂A = Δ·Ā and the B̄ of the chosen discretisation; dΔraw = dΔ·σ(Δraw +
+ * bias) with softplus; dz_t = dy_t·(C·h + D·u)_t·silu'(z_t); dh0 = Ā_0 ⊙ λ_0.
+ * Source: the backward pass recomputes the intermediate states rather than
+ * storing them ("Mamba and selective state spaces, from first principles",
+ * "The hardware-aware scan"; erikxu.me notes, "GPU Memory Hierarchy").  The
+ * pages give no formulas: these are the derivatives of the forward operation
+ * above.
+ *
+ * The forward inputs are those of ssm_scan_fwd (same meaning and layout); y
+ * itself is not needed.  All pointers are device pointers aligned to their
+ * element size (4 bytes for fp32); workspace 16-byte aligned.  The library
+ * zeroes dB, dC, dA, dDskip and ddelta_bias and accumulates into them on the
+ * device, so their values are sums in an unspecified order.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int64_t batch, dim, dstate, seqlen;   /* as in ssm_scan_params; dstate <= 16 */
+    ssm_dtype io_dtype;                   /* dtype of u, delta, z, B, C, dy, du, ddelta, dz */
+    const void *u, *delta, *z, *B, *C;    /* the forward inputs; z may be NULL */
+    const float *A, *Dskip, *delta_bias;  /* as in ssm_scan_params (NULL = 0 for the last two) */
+    int delta_softplus, zoh;              /* as in ssm_scan_params */
+    const float *h0;                      /* b × D × N fp32 initial state; NULL = zeros */
+    const void *dy;                       /* b × D × L, io_dtype: ∂loss/∂y */
+    const float *dhL;                     /* b × D × N fp32: ∂loss/∂hL; NULL = 0 */
+    void *du, *ddelta;                    /* out: b × D × L, io_dtype */
+    void *dz;                             /* out: b × D × L, io_dtype; NULL = not written */
+    float *dB, *dC;                       /* out: b × N × L fp32 */
+    float *dA;                            /* out: D × N fp32 */
+    float *dDskip, *ddelta_bias;          /* out: D fp32; NULL = not computed */
+    float *dh0;                           /* out: b × D × N fp32; NULL = not written */
+    void *workspace;                      /* >= ssm_scan_bwd_workspace_size(...) bytes */
+    size_t workspace_bytes;
+    int64_t chunk_len;                    /* 0 = automatic (256); else a multiple of 16 */
+} ssm_scan_bwd_params;
+
+/* Bytes of workspace ssm_scan_bwd needs: the status word and work counters,
+ * two chained hand-off states of b × D × N fp32, and the recurrence state at
+ * every 16th token (4 bytes per (b, d, t) element for N = 16).  0 for invalid
+ * sizes. */
+size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params *p);
+
+/* The backward scan: two launches on `stream` (a checkpoint pass and the
+ * reverse pass) after clearing the accumulated outputs.  Device-side wait
+ * failures are reported through ssm_workspace_status on this workspace. */
+ssm_status ssm_scan_bwd(const ssm_scan_bwd_params *p, ssm_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The short convolution in front of the SSM.
  *
  * Operation, per batch b, channel d and token t (W = width):

@@ -143,6 +143,86 @@ def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, *,
     return y
 
 
+def bwd_params(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, h0=None, dhL=None, *,
+               du, ddelta, dB, dC, dA, dz=None, dD=None, ddelta_bias=None, dh0=None,
+               delta_softplus=True, zoh=False, chunk_len=0, workspace=None) -> capi.BwdParams:
+    """Validate tensors and build the backward scan's C parameter struct."""
+    if u.dtype not in _DT:
+        raise ValueError(f"unsupported I/O dtype {u.dtype}")
+    dev = u.device
+    b, dim, L = u.shape
+    N = A.shape[1]
+    io = u.dtype
+    f32 = torch.float32
+    for t, name, shape, dt in ((u, "u", (b, dim, L), io), (delta, "delta", (b, dim, L), io),
+                               (B, "B", (b, N, L), io), (C, "C", (b, N, L), io), (dy, "dy", (b, dim, L), io),
+                               (A, "A", (dim, N), f32), (du, "du", (b, dim, L), io),
+                               (ddelta, "ddelta", (b, dim, L), io), (dB, "dB", (b, N, L), f32),
+                               (dC, "dC", (b, N, L), f32), (dA, "dA", (dim, N), f32)):
+        _need(t, name, shape, dt, dev)
+    for t, name, shape, dt in ((z, "z", (b, dim, L), io), (D, "D", (dim,), f32),
+                               (delta_bias, "delta_bias", (dim,), f32), (h0, "h0", (b, dim, N), f32),
+                               (dhL, "dhL", (b, dim, N), f32), (dz, "dz", (b, dim, L), io),
+                               (dD, "dD", (dim,), f32), (ddelta_bias, "ddelta_bias", (dim,), f32),
+                               (dh0, "dh0", (b, dim, N), f32)):
+        _opt(t, name, shape, dt, dev)
+    p = capi.BwdParams()
+    p.batch, p.dim, p.dstate, p.seqlen = b, dim, N, L
+    p.io_dtype = _DT[io]
+    p.u, p.delta, p.z, p.B, p.C = _ptr(u), _ptr(delta), _ptr(z), _ptr(B), _ptr(C)
+    p.A, p.Dskip, p.delta_bias = _ptr(A), _ptr(D), _ptr(delta_bias)
+    p.delta_softplus = int(bool(delta_softplus))
+    p.zoh = int(bool(zoh))
+    p.h0, p.dy, p.dhL = _ptr(h0), _ptr(dy), _ptr(dhL)
+    p.du, p.ddelta, p.dz = _ptr(du), _ptr(ddelta), _ptr(dz)
+    p.dB, p.dC, p.dA = _ptr(dB), _ptr(dC), _ptr(dA)
+    p.dDskip, p.ddelta_bias, p.dh0 = _ptr(dD), _ptr(ddelta_bias), _ptr(dh0)
+    p.chunk_len = int(chunk_len)
+    if workspace is not None:
+        p.workspace = workspace.data_ptr()
+        p.workspace_bytes = workspace.numel() * workspace.element_size()
+    return p
+
+
+def bwd_workspace_bytes(batch, dim, dstate, seqlen, chunk_len=0) -> int:
+    p = capi.BwdParams()
+    p.batch, p.dim, p.dstate, p.seqlen = batch, dim, dstate, seqlen
+    p.chunk_len = int(chunk_len)
+    n = capi.ssm_scan_bwd_workspace_size(p)
+    if n == 0:
+        raise ValueError("invalid backward scan sizes")
+    return n
+
+
+def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, h0=None, dhL=None, *,
+             delta_softplus=True, zoh=False, chunk_len=0, workspace=None, stream=None) -> dict:
+    """Gradients of scan_fwd for upstream dy (and dhL).  Returns a dict with du,
+    ddelta, dz (None without z), dB, dC, dA, dD, ddelta_bias (None when D /
+    delta_bias are None) and dh0 (None without h0); dB, dC, dA, dD and
+    ddelta_bias are fp32."""
+    b, dim, L = u.shape
+    N = A.shape[1]
+    dev = u.device
+    f32 = torch.float32
+    out = dict(du=torch.empty_like(u), ddelta=torch.empty_like(delta),
+               dz=torch.empty_like(z) if z is not None else None,
+               dB=torch.empty((b, N, L), dtype=f32, device=dev), dC=torch.empty((b, N, L), dtype=f32, device=dev),
+               dA=torch.empty((dim, N), dtype=f32, device=dev),
+               dD=torch.empty(dim, dtype=f32, device=dev) if D is not None else None,
+               ddelta_bias=torch.empty(dim, dtype=f32, device=dev) if delta_bias is not None else None,
+               dh0=torch.empty((b, dim, N), dtype=f32, device=dev) if h0 is not None else None)
+    if workspace is None:
+        workspace = torch.empty(bwd_workspace_bytes(b, dim, N, L, chunk_len), dtype=torch.uint8, device=dev)
+    p = bwd_params(u, delta, A, B, C, dy, D, z, delta_bias, h0, dhL, du=out["du"], ddelta=out["ddelta"],
+                   dB=out["dB"], dC=out["dC"], dA=out["dA"], dz=out["dz"], dD=out["dD"],
+                   ddelta_bias=out["ddelta_bias"], dh0=out["dh0"], delta_softplus=delta_softplus, zoh=zoh,
+                   chunk_len=chunk_len, workspace=workspace)
+    st = torch.cuda.current_stream(dev).cuda_stream if stream is None else stream
+    capi.check(capi.ssm_scan_bwd(p, st), "ssm_scan_bwd")
+    out["workspace"] = workspace
+    return out
+
+
 def conv_params(x, weight, bias=None, state_in=None, *, u, state_out=None, silu=True) -> capi.ConvParams:
     """Validate tensors and build the convolution's C parameter struct."""
     if x.dtype not in _DT:

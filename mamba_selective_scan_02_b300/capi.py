@@ -47,6 +47,21 @@ class StepParams(ctypes.Structure):
     ]
 
 
+class BwdParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("dstate", _i64), ("seqlen", _i64),
+        ("io_dtype", ctypes.c_int),
+        ("u", _vp), ("delta", _vp), ("z", _vp), ("B", _vp), ("C", _vp),
+        ("A", _vp), ("Dskip", _vp), ("delta_bias", _vp),
+        ("delta_softplus", ctypes.c_int), ("zoh", ctypes.c_int),
+        ("h0", _vp), ("dy", _vp), ("dhL", _vp),
+        ("du", _vp), ("ddelta", _vp), ("dz", _vp), ("dB", _vp), ("dC", _vp), ("dA", _vp),
+        ("dDskip", _vp), ("ddelta_bias", _vp), ("dh0", _vp),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("chunk_len", _i64),
+    ]
+
+
 class ConvParams(ctypes.Structure):
     _fields_ = [
         ("batch", _i64), ("dim", _i64), ("seqlen", _i64), ("width", _i64),
@@ -96,6 +111,10 @@ def lib():
             L.ssm_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ScanParams), _vp]
             L.ssm_state_update.restype = ctypes.c_int
             L.ssm_state_update.argtypes = [ctypes.POINTER(StepParams), _vp]
+            L.ssm_scan_bwd_workspace_size.restype = ctypes.c_size_t
+            L.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(BwdParams)]
+            L.ssm_scan_bwd.restype = ctypes.c_int
+            L.ssm_scan_bwd.argtypes = [ctypes.POINTER(BwdParams), _vp]
             L.ssm_conv1d_fwd.restype = ctypes.c_int
             L.ssm_conv1d_fwd.argtypes = [ctypes.POINTER(ConvParams), _vp]
             L.ssm_conv1d_step.restype = ctypes.c_int
@@ -148,6 +167,14 @@ def ssm_scan_fwd_noalloc(p: ScanParams, stream: int) -> int:
 
 def ssm_state_update(p: StepParams, stream: int) -> int:
     return lib().ssm_state_update(ctypes.byref(p), stream)
+
+
+def ssm_scan_bwd_workspace_size(p: BwdParams) -> int:
+    return lib().ssm_scan_bwd_workspace_size(ctypes.byref(p))
+
+
+def ssm_scan_bwd(p: BwdParams, stream: int) -> int:
+    return lib().ssm_scan_bwd(ctypes.byref(p), stream)
 
 
 def ssm_conv1d_fwd(p: ConvParams, stream: int) -> int:

@@ -64,9 +64,138 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
+bool bwd_sizes_ok(const ssm_scan_bwd_params *p) {
+    if (!p) return false;
+    if (p->batch < 1 || p->dim < 1 || p->seqlen < 1 || p->dstate < 1) return false;
+    if (p->batch > 65535 || p->dim > (1 << 30) || p->seqlen > INT32_MAX / 2) return false;
+    if (p->chunk_len < 0 || (p->chunk_len > 0 && p->chunk_len % ssm::kBwdTile != 0)) return false;
+    return true;
+}
+
+struct BwdLayout {
+    int64_t groups, ntiles, chunk_len, nchunks;
+    size_t flags_fwd, flags_rev, carry_fwd, carry_rev, ckpt, zero_bytes, total;
+};
+
+// Backward workspace: the 256-byte header (status word, two work counters),
+// one int flag per channel group for each pass, the two b × D × N fp32
+// hand-off states, then the state at every tile start, [group][tile][256]
+// fp32.  The header and the flags are cleared before every call.
+BwdLayout bwd_layout(const ssm_scan_bwd_params *p) {
+    BwdLayout l;
+    const int cpw = ssm::bwd_cpw(p->dstate);
+    l.groups = p->batch * ((p->dim + cpw - 1) / cpw);
+    l.ntiles = (p->seqlen + ssm::kBwdTile - 1) / ssm::kBwdTile;
+    l.chunk_len = p->chunk_len > 0 ? p->chunk_len : ssm::kBwdChunk;
+    l.nchunks = (p->seqlen + l.chunk_len - 1) / l.chunk_len;
+    const size_t flag_bytes = align256((size_t)l.groups * sizeof(int));
+    const size_t bdn = align256((size_t)p->batch * p->dim * p->dstate * sizeof(float));
+    l.flags_fwd = kHeader;
+    l.flags_rev = l.flags_fwd + flag_bytes;
+    l.zero_bytes = l.flags_rev + flag_bytes;
+    l.carry_fwd = l.zero_bytes;
+    l.carry_rev = l.carry_fwd + bdn;
+    l.ckpt = l.carry_rev + bdn;
+    l.total = l.ckpt + (size_t)l.groups * l.ntiles * 256 * sizeof(float);
+    return l;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params *p) {
+    if (!bwd_sizes_ok(p)) return 0;
+    return bwd_layout(p).total;
+}
+
+ssm_status ssm_scan_bwd(const ssm_scan_bwd_params *p, ssm_stream_t stream) {
+    if (!bwd_sizes_ok(p)) return SSM_ERR_INVALID_ARG;
+    if (p->io_dtype != SSM_F32 && p->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (p->dstate > SSM_MAX_DSTATE) return SSM_ERR_UNSUPPORTED;
+    if (p->zoh != 0 && p->zoh != 1) return SSM_ERR_INVALID_ARG;
+    if (p->delta_softplus != 0 && p->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (!p->u || !p->delta || !p->B || !p->C || !p->A || !p->dy || !p->du || !p->ddelta || !p->dB || !p->dC ||
+        !p->dA || !p->workspace)
+        return SSM_ERR_INVALID_ARG;
+    const size_t es = p->io_dtype == SSM_BF16 ? 2 : 4;
+    const void *aio[] = {p->u, p->delta, p->z, p->B, p->C, p->dy, p->du, p->ddelta, p->dz};
+    for (const void *q : aio)
+        if (q && (reinterpret_cast<uintptr_t>(q) % es) != 0) return SSM_ERR_INVALID_ARG;
+    const void *a4[] = {p->A, p->Dskip, p->delta_bias, p->h0, p->dhL, p->dB, p->dC, p->dA, p->dDskip,
+                        p->ddelta_bias, p->dh0};
+    for (const void *q : a4)
+        if (q && !aligned4(q)) return SSM_ERR_INVALID_ARG;
+    if (!aligned16(p->workspace)) return SSM_ERR_INVALID_ARG;
+    const size_t seq = (size_t)p->batch * p->dim * p->seqlen * es;
+    const size_t bc = (size_t)p->batch * p->dstate * p->seqlen * es;
+    const size_t bcf = (size_t)p->batch * p->dstate * p->seqlen * 4;
+    const void *ins[] = {p->u, p->delta, p->z, p->dy};
+    const void *outs[] = {p->du, p->ddelta, p->dz};
+    for (const void *o : outs) {
+        for (const void *i : ins)
+            if (overlaps(o, seq, i, seq)) return SSM_ERR_INVALID_ARG;
+        if (overlaps(o, seq, p->B, bc) || overlaps(o, seq, p->C, bc)) return SSM_ERR_INVALID_ARG;
+    }
+    if (overlaps(p->du, seq, p->ddelta, seq) || overlaps(p->du, seq, p->dz, seq) ||
+        overlaps(p->ddelta, seq, p->dz, seq) || overlaps(p->dB, bcf, p->dC, bcf) || overlaps(p->dB, bcf, p->B, bc) ||
+        overlaps(p->dC, bcf, p->C, bc))
+        return SSM_ERR_INVALID_ARG;
+    const BwdLayout l = bwd_layout(p);
+    if (p->workspace_bytes < l.total) return SSM_ERR_INVALID_ARG;
+    if (l.groups * l.nchunks > INT32_MAX / 2 || l.groups * l.ntiles > INT32_MAX / 2) return SSM_ERR_UNSUPPORTED;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(p->workspace);
+    if (cudaMemsetAsync(ws, 0, l.zero_bytes, st) != cudaSuccess) return SSM_ERR_CUDA;
+    const size_t dn = (size_t)p->dim * p->dstate * sizeof(float);
+    if (cudaMemsetAsync(p->dB, 0, bcf, st) != cudaSuccess || cudaMemsetAsync(p->dC, 0, bcf, st) != cudaSuccess ||
+        cudaMemsetAsync(p->dA, 0, dn, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (p->dDskip && cudaMemsetAsync(p->dDskip, 0, p->dim * sizeof(float), st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (p->ddelta_bias && cudaMemsetAsync(p->ddelta_bias, 0, p->dim * sizeof(float), st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+
+    ssm::BwdArgs a;
+    a.batch = (int)p->batch;
+    a.dim = (int)p->dim;
+    a.dstate = (int)p->dstate;
+    a.seqlen = (int)p->seqlen;
+    a.u = p->u;
+    a.delta = p->delta;
+    a.z = p->z;
+    a.B = p->B;
+    a.C = p->C;
+    a.dy = p->dy;
+    a.A = p->A;
+    a.Dskip = p->Dskip;
+    a.bias = p->delta_bias;
+    a.h0 = p->h0;
+    a.dhL = p->dhL;
+    a.delta_softplus = p->delta_softplus;
+    a.zoh = p->zoh;
+    a.du = p->du;
+    a.ddelta = p->ddelta;
+    a.dz = p->z ? p->dz : nullptr;
+    a.dB = p->dB;
+    a.dC = p->dC;
+    a.dA = p->dA;
+    a.dDskip = p->dDskip;
+    a.dbias = p->ddelta_bias;
+    a.dh0 = p->dh0;
+    a.status = reinterpret_cast<int *>(ws);
+    a.tickets = reinterpret_cast<int *>(ws) + 1;
+    a.flags_fwd = reinterpret_cast<int *>(ws + l.flags_fwd);
+    a.flags_rev = reinterpret_cast<int *>(ws + l.flags_rev);
+    a.carry_fwd = reinterpret_cast<float *>(ws + l.carry_fwd);
+    a.carry_rev = reinterpret_cast<float *>(ws + l.carry_rev);
+    a.ckpt = reinterpret_cast<float *>(ws + l.ckpt);
+    a.chunk_len = (int)l.chunk_len;
+    a.nchunks = (int)l.nchunks;
+    a.groups = (int)l.groups;
+    a.ntiles = (int)l.ntiles;
+    return ssm::bwd_launch(a, p->io_dtype == SSM_BF16, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
 
 size_t ssm_scan_workspace_size(const ssm_scan_params *p) {
     if (!scan_sizes_ok(p)) return 0;

@@ -1,0 +1,706 @@
+// scan_bwd.cu — the backward selective scan for sm_103a: gradients of
+//   Δ = softplus(Δraw + bias), Ā = exp(Δ·A), B̄ = Δ·B (or the exact hold),
+//   h_t = Ā_t h_{t−1} + B̄_t u_t,  y_t = (C_t·h_t + D u_t)·silu(z_t)
+// with respect to u, Δraw, z, B, C, A, D, bias and h0, for an upstream
+// gradient dy (and dhL on the final state).
+//
+// "The hardware-aware scan" on "Mamba and selective state spaces, from first
+// principles" (and "GPU Memory Hierarchy" in the erikxu.me notes) recomputes
+// the intermediate states in the backward pass instead of storing them.  The
+// adjoint runs backwards in time,
+//   λ_t = C_t ŷ_t + Ā_{t+1} λ_{t+1},   λ_{L−1} starts from dhL,  ŷ_t = dy_t·silu(z_t),
+// and every gradient is read off λ_t, h_{t−1} and the per-token terms.
+//
+// Design (B300-first).  Lanes own channels and states as in the forward scan
+// (two lanes per channel with eight states each for N ≤ 16, one lane per
+// channel for N ≤ 8), and warps are persistent over (channel group, chunk)
+// work items.  Two launches:
+//   1. checkpoint pass: the forward recurrence, chunk k starting from the state
+//      chunk k−1 hands over (a flag per group, bounded spin), writing the state
+//      at every 16-token tile start to the workspace — the only h kept;
+//   2. reverse pass: chunks in reverse order, chunk k starting from the adjoint
+//      chunk k+1 hands over.  Per tile it recomputes the 16 states from the
+//      checkpoint into shared memory, then walks the tile backwards.
+// dB and dC sum over channels: per token a warp folds dB over its channels
+// with a transposed butterfly (each shuffle halves the values a lane holds);
+// dC = Σ ŷ·h is formed per tile from the stored states; the tile's [16 × N]
+// sums are added to memory.  dA, dD and dbias sum over tokens in registers
+// and are added once per item.  Each tile's global loads are issued one tile
+// ahead, into registers.
+#include <algorithm>
+
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+namespace {
+
+constexpr int TS = kBwdTile;            // tokens per tile
+constexpr int TSP = TS + 1;             // padded row of the per-channel term arrays
+constexpr int SPT = 8;                  // states per lane
+constexpr int kBwdFlagLimit = 1 << 24;  // polls of a neighbour's flag before giving up
+constexpr int kBwdWarpsPerSM = 8;
+
+__device__ __forceinline__ int ld_acquire_b(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_b(int *p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.0f + ex2(-x * kLog2e)); }
+
+// ψ(x) = (e^x − φ(x))/x with φ(x) = (e^x − 1)/x: ∂B̄/∂A = B·Δ²·ψ(ΔA) under the
+// exact hold.  Taylor series Σ_{m≥2} (m−1)/m! x^{m−2} for |x| < 1/4 (next term
+// x^6/6720 < 4e-8), the closed form above, where the cancellation is mild.
+__device__ __forceinline__ float zoh_psi(float x, float abar, float phi) {
+    float p = fmaf(x, 1.0f / 840.0f, 1.0f / 144.0f);
+    p = fmaf(x, p, 1.0f / 30.0f);
+    p = fmaf(x, p, 1.0f / 8.0f);
+    p = fmaf(x, p, 1.0f / 3.0f);
+    p = fmaf(x, p, 0.5f);
+    return fabsf(x) < 0.25f ? p : __fdividef(abar - phi, x);
+}
+
+template <int NG> struct BwdShape {
+    static constexpr int CPW = 32 / NG;   // channels per warp
+    static constexpr int NP = SPT * NG;   // states covered
+    static constexpr int OWN = TS / NG;   // tokens whose terms a lane stages
+};
+
+// Eight consecutive tokens of a row in the I/O type, zero beyond L.  VEC: one
+// (bf16) or two (fp32) 16-byte loads — the row pitch and t are multiples of 8;
+// otherwise bounded scalar loads.  Kept raw until staged, so a prefetched tile
+// costs 4 (bf16) or 8 (fp32) registers per 8 tokens.
+template <typename T> struct R8 {
+    static constexpr int W = 8 * (int)sizeof(T) / 16;   // 16-byte words
+    uint4 w[W];
+    template <bool VEC> __device__ __forceinline__ void load(const T *row, int t, int L) {
+        if (VEC) {
+            if (t < L) {
+#pragma unroll
+                for (int i = 0; i < W; ++i) w[i] = __ldg(reinterpret_cast<const uint4 *>(row + t) + i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < W; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        } else {
+            T *v = reinterpret_cast<T *>(w);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = (t + i < L) ? row[t + i] : IO<T>::from_f(0.f);
+        }
+    }
+    __device__ __forceinline__ float at(int i) const { return IO<T>::to_f(reinterpret_cast<const T *>(w)[i]); }
+};
+
+// One tile of B or C rows: lane i < 2N holds row n = i / 2, tokens 8·(i % 2) .. +7.
+template <typename T, bool VEC>
+__device__ __forceinline__ void fetch_rows(R8<T> &r, const T *src, int b, int N, int L, int t0, int lane) {
+    if (lane < 2 * N) r.template load<VEC>(src + ((size_t)b * N + (lane >> 1)) * L, t0 + 8 * (lane & 1), L);
+}
+// ... into fp32 token-major rows [TS][NP] (entries n >= N stay zero).
+template <typename T, int NP>
+__device__ __forceinline__ void store_rows(float *dst, const R8<T> &r, int N, int lane) {
+    if (lane < 2 * N) {
+        const int n = lane >> 1, tt = 8 * (lane & 1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[(tt + i) * NP + n] = r.at(i);
+    }
+}
+
+struct BwdItem {
+    int grp, k, b, d0;
+};
+
+// ------------------------------------------------------------------ pass 1
+template <typename T, int NG, bool ZOH, bool VEC>
+__global__ void __launch_bounds__(32)
+bwd_ckpt_kernel(const BwdArgs a) {
+    using S = BwdShape<NG>;
+    constexpr int CPW = S::CPW, NP = S::NP, OWN = S::OWN, NQ = SPT / 2;
+    constexpr unsigned FULL = 0xffffffffu;
+    __shared__ __align__(16) float Bs[TS * NP];
+    __shared__ float Dl[CPW * TSP], Du[CPW * TSP];
+
+    const int lane = threadIdx.x, c = lane / NG, g = lane % NG;
+    const int D = a.dim, N = a.dstate, L = a.seqlen, K = a.nchunks;
+    const int gpb = (D + CPW - 1) / CPW;
+    const int items = a.groups * K;
+    for (int i = lane; i < TS * NP; i += 32) Bs[i] = 0.f;
+
+    while (true) {
+        int tk = 0;
+        if (lane == 0) tk = atomicAdd(a.tickets, 1);
+        tk = __shfl_sync(FULL, tk, 0);
+        if (tk >= items) break;
+        BwdItem it;
+        it.k = tk / a.groups;
+        it.grp = tk % a.groups;
+        it.b = it.grp / gpb;
+        it.d0 = (it.grp % gpb) * CPW;
+        const int d = it.d0 + c;
+        const bool live = d < D;
+
+        float2 A2[NQ], h[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            float av[2] = {0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int n = SPT * g + 2 * q + j;
+                if (live && n < N) av[j] = a.A[(size_t)d * N + n] * kLog2e;
+            }
+            A2[q] = make_float2(av[0], av[1]);
+            h[q] = make_float2(0.f, 0.f);
+        }
+        const float bias = (live && a.bias) ? a.bias[d] : 0.f;
+        const float *src = nullptr;
+        bool cg = false;
+        if (it.k == 0) {
+            src = a.h0 ? a.h0 + ((size_t)it.b * D + d) * N : nullptr;
+        } else {
+            if (lane == 0) {
+                int polls = 0;
+                while (ld_acquire_b(a.flags_fwd + it.grp) < it.k && ++polls < kBwdFlagLimit) __nanosleep(64);
+                if (polls >= kBwdFlagLimit) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
+            }
+            __syncwarp();
+            (void)ld_acquire_b(a.flags_fwd + it.grp);
+            src = a.carry_fwd + ((size_t)it.b * D + d) * N;
+            cg = true;
+        }
+        if (src && live) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const int n = SPT * g + 2 * q;
+                float hx = 0.f, hy = 0.f;
+                if (n < N) hx = cg ? __ldcg(src + n) : src[n];
+                if (n + 1 < N) hy = cg ? __ldcg(src + n + 1) : src[n + 1];
+                h[q] = make_float2(hx, hy);
+            }
+        }
+
+        const int tb = it.k * a.chunk_len, te = min(L, tb + a.chunk_len);
+        const T *urow = static_cast<const T *>(a.u) + ((size_t)it.b * D + (live ? d : 0)) * L;
+        const T *drow = static_cast<const T *>(a.delta) + ((size_t)it.b * D + (live ? d : 0)) * L;
+        // the tile's global loads, issued one tile ahead of their use
+        struct Pre {
+            R8<T> b, u[OWN / 8], d[OWN / 8];
+        };
+        auto fetch = [&](int t0, Pre &f) {
+            fetch_rows<T, VEC>(f.b, static_cast<const T *>(a.B), it.b, N, L, t0, lane);
+#pragma unroll
+            for (int h8 = 0; h8 < OWN / 8; ++h8) {
+                f.u[h8].template load<VEC>(urow, t0 + OWN * g + 8 * h8, L);
+                f.d[h8].template load<VEC>(drow, t0 + OWN * g + 8 * h8, L);
+            }
+        };
+        Pre cur;
+        fetch(tb, cur);
+        for (int t0 = tb; t0 < te; t0 += TS) {
+            // the state entering this tile is its checkpoint
+            float4 *ck = reinterpret_cast<float4 *>(a.ckpt) + ((size_t)it.grp * a.ntiles + t0 / TS) * 64;
+            ck[lane] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+            ck[32 + lane] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
+
+            __syncwarp();
+            store_rows<T, NP>(Bs, cur.b, N, lane);
+#pragma unroll
+            for (int h8 = 0; h8 < OWN / 8; ++h8) {
+                const int j0 = OWN * g + 8 * h8, t = t0 + j0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float dl = 0.f;
+                    if (live && t + i < L) {
+                        const float x = cur.d[h8].at(i) + bias;
+                        dl = a.delta_softplus ? softplus_poly(x) : x;
+                    }
+                    Dl[c * TSP + j0 + i] = dl;
+                    Du[c * TSP + j0 + i] = dl * cur.u[h8].at(i);
+                }
+            }
+            __syncwarp();
+            if (t0 + TS < te) fetch(t0 + TS, cur);
+#pragma unroll 4
+            for (int t = 0; t < TS; ++t) {
+                const float dl = Dl[c * TSP + t], du = Du[c * TSP + t];
+                const float4 b0 = *reinterpret_cast<const float4 *>(Bs + t * NP + SPT * g);
+                const float4 b1 = *reinterpret_cast<const float4 *>(Bs + t * NP + SPT * g + 4);
+                const float2 bq[NQ] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                                       make_float2(b1.z, b1.w)};
+                const float2 d2 = make_float2(dl, dl), du2 = make_float2(du, du);
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const float2 x = __fmul2_rn(d2, A2[q]);
+                    const float2 ab = make_float2(ex2(x.x), ex2(x.y));
+                    float2 bb = __fmul2_rn(bq[q], du2);
+                    if (ZOH) {
+                        const float2 xn = __fmul2_rn(x, make_float2(kLn2, kLn2));
+                        bb = __fmul2_rn(bb, make_float2(zoh_phi(xn.x, ab.x), zoh_phi(xn.y, ab.y)));
+                    }
+                    h[q] = __ffma2_rn(ab, h[q], bb);
+                }
+            }
+        }
+        if (it.k + 1 < K) {
+            if (live) {
+                float *dst = a.carry_fwd + ((size_t)it.b * D + d) * N;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const int n = SPT * g + 2 * q;
+                    if (n < N) dst[n] = h[q].x;
+                    if (n + 1 < N) dst[n + 1] = h[q].y;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) st_release_b(a.flags_fwd + it.grp, it.k + 1);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ pass 2
+template <int NG> struct RevSmem {
+    static constexpr int CPW = BwdShape<NG>::CPW, NP = BwdShape<NG>::NP;
+    float4 Hs[TS * 2 * 32];                 // state after token t: [t][half][lane]
+    float Bs[TS * NP], Cs[TS * NP];         // fp32 token-major rows
+    float acc[TS * 2 * NP];                 // [t][dB | dC][n]: the tile's channel sums
+    float Dl[CPW * TSP], Du[CPW * TSP], U[CPW * TSP], Sg[CPW * TSP], Yh[CPW * TSP], Gp[CPW * TSP],
+        Sp[CPW * TSP];                      // per-channel token terms
+    float Odu[CPW * TSP], Odd[CPW * TSP], Odz[CPW * TSP];  // outputs of the tile
+};
+
+template <typename T, int NG, bool HAS_Z, bool ZOH, bool VEC>
+__global__ void __launch_bounds__(32)
+bwd_rev_kernel(const BwdArgs a) {
+    using S = BwdShape<NG>;
+    constexpr int CPW = S::CPW, NP = S::NP, OWN = S::OWN, NQ = SPT / 2;
+    constexpr unsigned FULL = 0xffffffffu;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    RevSmem<NG> &sm = *reinterpret_cast<RevSmem<NG> *>(smem_raw);
+
+    const int lane = threadIdx.x, c = lane / NG, g = lane % NG;
+    const int D = a.dim, N = a.dstate, L = a.seqlen, K = a.nchunks;
+    const int gpb = (D + CPW - 1) / CPW;
+    const int items = a.groups * K;
+    for (int i = lane; i < TS * NP; i += 32) sm.Bs[i] = sm.Cs[i] = 0.f;
+
+    while (true) {
+        int tk = 0;
+        if (lane == 0) tk = atomicAdd(a.tickets + 1, 1);
+        tk = __shfl_sync(FULL, tk, 0);
+        if (tk >= items) break;
+        BwdItem it;
+        const int r = tk / a.groups;          // chunks already done after this one
+        it.k = K - 1 - r;
+        it.grp = tk % a.groups;
+        it.b = it.grp / gpb;
+        it.d0 = (it.grp % gpb) * CPW;
+        const int d = it.d0 + c;
+        const bool live = d < D;
+
+        float2 A2[NQ], Af[NQ], lam[NQ], dA[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            float av[2] = {0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int n = SPT * g + 2 * q + j;
+                if (live && n < N) av[j] = a.A[(size_t)d * N + n];
+            }
+            Af[q] = make_float2(av[0], av[1]);
+            A2[q] = make_float2(av[0] * kLog2e, av[1] * kLog2e);
+            lam[q] = dA[q] = make_float2(0.f, 0.f);
+        }
+        const float bias = (live && a.bias) ? a.bias[d] : 0.f;
+        const float skip = (live && a.Dskip) ? a.Dskip[d] : 0.f;
+        float dD_acc = 0.f, db_acc = 0.f;
+
+        // the adjoint entering the chunk's last token from the right
+        const float *src = nullptr;
+        bool cg = false;
+        if (r == 0) {
+            src = a.dhL ? a.dhL + ((size_t)it.b * D + d) * N : nullptr;
+        } else {
+            if (lane == 0) {
+                int polls = 0;
+                while (ld_acquire_b(a.flags_rev + it.grp) < r && ++polls < kBwdFlagLimit) __nanosleep(64);
+                if (polls >= kBwdFlagLimit) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
+            }
+            __syncwarp();
+            (void)ld_acquire_b(a.flags_rev + it.grp);
+            src = a.carry_rev + ((size_t)it.b * D + d) * N;
+            cg = true;
+        }
+        if (src && live) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const int n = SPT * g + 2 * q;
+                float lx = 0.f, ly = 0.f;
+                if (n < N) lx = cg ? __ldcg(src + n) : src[n];
+                if (n + 1 < N) ly = cg ? __ldcg(src + n + 1) : src[n + 1];
+                lam[q] = make_float2(lx, ly);
+            }
+        }
+
+        const size_t rowoff = ((size_t)it.b * D + (live ? d : 0)) * L;
+        const T *urow = static_cast<const T *>(a.u) + rowoff;
+        const T *drow = static_cast<const T *>(a.delta) + rowoff;
+        const T *zrow = HAS_Z ? static_cast<const T *>(a.z) + rowoff : nullptr;
+        const T *dyrow = static_cast<const T *>(a.dy) + rowoff;
+        const int tb = it.k * a.chunk_len, te = min(L, tb + a.chunk_len);
+        const int nt = (te - tb + TS - 1) / TS;
+
+        // a tile's global loads, issued one tile ahead of their use
+        struct Pre {
+            R8<T> b, c, u[OWN / 8], d[OWN / 8], z[HAS_Z ? OWN / 8 : 1], y[OWN / 8];
+        };
+        auto fetch = [&](int t0, Pre &f) {
+            fetch_rows<T, VEC>(f.b, static_cast<const T *>(a.B), it.b, N, L, t0, lane);
+            fetch_rows<T, VEC>(f.c, static_cast<const T *>(a.C), it.b, N, L, t0, lane);
+#pragma unroll
+            for (int h8 = 0; h8 < OWN / 8; ++h8) {
+                const int t = t0 + OWN * g + 8 * h8;
+                f.u[h8].template load<VEC>(urow, t, L);
+                f.d[h8].template load<VEC>(drow, t, L);
+                f.y[h8].template load<VEC>(dyrow, t, L);
+                if (HAS_Z) f.z[h8].template load<VEC>(zrow, t, L);
+            }
+        };
+        Pre cur;
+        fetch(tb + (nt - 1) * TS, cur);
+
+        for (int tt = nt - 1; tt >= 0; --tt) {
+            const int t0 = tb + tt * TS;
+            const float4 *ck = reinterpret_cast<const float4 *>(a.ckpt) + ((size_t)it.grp * a.ntiles + t0 / TS) * 64;
+            const float4 hs0 = ck[lane], hs1 = ck[32 + lane];
+            const float2 hstart[NQ] = {make_float2(hs0.x, hs0.y), make_float2(hs0.z, hs0.w),
+                                       make_float2(hs1.x, hs1.y), make_float2(hs1.z, hs1.w)};
+
+            // ---- stage B, C and the per-channel token terms
+            __syncwarp();
+            store_rows<T, NP>(sm.Bs, cur.b, N, lane);
+            store_rows<T, NP>(sm.Cs, cur.c, N, lane);
+#pragma unroll
+            for (int h8 = 0; h8 < OWN / 8; ++h8) {
+                const int j0 = OWN * g + 8 * h8, t = t0 + j0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = c * TSP + j0 + i;
+                    const bool v = live && t + i < L;
+                    float dl = 0.f, sg = 0.f, uu = 0.f, yh = 0.f, gp = 0.f;
+                    if (v) {
+                        const float x = cur.d[h8].at(i) + bias, yv = cur.y[h8].at(i);
+                        dl = a.delta_softplus ? softplus_poly(x) : x;
+                        sg = a.delta_softplus ? sigmoid_f(x) : 1.f;
+                        uu = cur.u[h8].at(i);
+                        if (HAS_Z) {
+                            const float zv = cur.z[h8].at(i), sz = sigmoid_f(zv);
+                            yh = yv * zv * sz;
+                            gp = yv * sz * fmaf(zv, 1.f - sz, 1.f);  // dy · silu'(z)
+                        } else {
+                            yh = yv;
+                        }
+                    }
+                    sm.Dl[e] = dl;
+                    sm.Du[e] = dl * uu;
+                    sm.U[e] = uu;
+                    sm.Sg[e] = sg;
+                    sm.Yh[e] = yh;
+                    sm.Gp[e] = gp;
+                }
+            }
+            __syncwarp();
+            if (tt > 0) fetch(t0 - TS, cur);
+
+            // ---- recompute the tile's states from its checkpoint
+            float2 h[NQ];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) h[q] = hstart[q];
+#pragma unroll 2
+            for (int t = 0; t < TS; ++t) {
+                const float dl = sm.Dl[c * TSP + t], du = sm.Du[c * TSP + t];
+                const float4 b0 = *reinterpret_cast<const float4 *>(sm.Bs + t * NP + SPT * g);
+                const float4 b1 = *reinterpret_cast<const float4 *>(sm.Bs + t * NP + SPT * g + 4);
+                const float4 c0 = *reinterpret_cast<const float4 *>(sm.Cs + t * NP + SPT * g);
+                const float4 c1 = *reinterpret_cast<const float4 *>(sm.Cs + t * NP + SPT * g + 4);
+                const float2 bq[NQ] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                                       make_float2(b1.z, b1.w)};
+                const float2 cq[NQ] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
+                                       make_float2(c1.z, c1.w)};
+                const float2 d2 = make_float2(dl, dl), du2 = make_float2(du, du);
+                float2 p2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const float2 x = __fmul2_rn(d2, A2[q]);
+                    const float2 ab = make_float2(ex2(x.x), ex2(x.y));
+                    float2 bb = __fmul2_rn(bq[q], du2);
+                    if (ZOH) {
+                        const float2 xn = __fmul2_rn(x, make_float2(kLn2, kLn2));
+                        bb = __fmul2_rn(bb, make_float2(zoh_phi(xn.x, ab.x), zoh_phi(xn.y, ab.y)));
+                    }
+                    h[q] = __ffma2_rn(ab, h[q], bb);
+                    p2 = __ffma2_rn(cq[q], h[q], p2);
+                }
+                sm.Hs[(t * 2) * 32 + lane] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+                sm.Hs[(t * 2 + 1) * 32 + lane] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
+                float p = p2.x + p2.y;
+                if (NG == 2) p += __shfl_xor_sync(FULL, p, 1);
+                if (g == 0) sm.Sp[c * TSP + t] = fmaf(skip, sm.U[c * TSP + t], p);  // C·h + D·u
+            }
+            __syncwarp();
+
+            // ---- dC of the tile: Σ over the warp's channels of ŷ·h, read back
+            // from the stored states (lane: one token, half of the states; the
+            // channel order is staggered by token against bank conflicts)
+            {
+                constexpr int HN = NP / 2;            // states per lane here
+                const int t = lane >> 1, hh = lane & 1;
+                float acc[HN];
+#pragma unroll
+                for (int j = 0; j < HN; ++j) acc[j] = 0.f;
+#pragma unroll 4
+                for (int i = 0; i < CPW; ++i) {
+                    const int cc = (i + t) % CPW;
+                    const float y = sm.Yh[cc * TSP + t];
+                    if (NG == 2) {
+                        const float4 p0 = sm.Hs[(t * 2) * 32 + 2 * cc + hh], p1 = sm.Hs[(t * 2 + 1) * 32 + 2 * cc + hh];
+                        acc[0] = fmaf(y, p0.x, acc[0]); acc[1] = fmaf(y, p0.y, acc[1]);
+                        acc[2 % HN] = fmaf(y, p0.z, acc[2 % HN]); acc[3 % HN] = fmaf(y, p0.w, acc[3 % HN]);
+                        acc[4 % HN] = fmaf(y, p1.x, acc[4 % HN]); acc[5 % HN] = fmaf(y, p1.y, acc[5 % HN]);
+                        acc[6 % HN] = fmaf(y, p1.z, acc[6 % HN]); acc[7 % HN] = fmaf(y, p1.w, acc[7 % HN]);
+                    } else {
+                        const float4 p0 = sm.Hs[(t * 2 + hh) * 32 + cc];
+                        acc[0] = fmaf(y, p0.x, acc[0]); acc[1] = fmaf(y, p0.y, acc[1]);
+                        acc[2 % HN] = fmaf(y, p0.z, acc[2 % HN]); acc[3 % HN] = fmaf(y, p0.w, acc[3 % HN]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < HN; ++j) sm.acc[(t * 2 + 1) * NP + HN * hh + j] = acc[j];
+            }
+
+            // ---- the adjoint, backwards through the tile
+            float2 hcur[NQ];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) hcur[q] = h[q];
+#pragma unroll 2
+            for (int t = TS - 1; t >= 0; --t) {
+                float2 hprev[NQ];
+                if (t > 0) {
+                    const float4 p0 = sm.Hs[((t - 1) * 2) * 32 + lane], p1 = sm.Hs[((t - 1) * 2 + 1) * 32 + lane];
+                    hprev[0] = make_float2(p0.x, p0.y);
+                    hprev[1] = make_float2(p0.z, p0.w);
+                    hprev[2] = make_float2(p1.x, p1.y);
+                    hprev[3] = make_float2(p1.z, p1.w);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) hprev[q] = hstart[q];
+                }
+                const int e = c * TSP + t;
+                const float yh = sm.Yh[e], dl = sm.Dl[e], uu = sm.U[e], du = sm.Du[e];
+                const float4 b0 = *reinterpret_cast<const float4 *>(sm.Bs + t * NP + SPT * g);
+                const float4 b1 = *reinterpret_cast<const float4 *>(sm.Bs + t * NP + SPT * g + 4);
+                const float4 c0 = *reinterpret_cast<const float4 *>(sm.Cs + t * NP + SPT * g);
+                const float4 c1 = *reinterpret_cast<const float4 *>(sm.Cs + t * NP + SPT * g + 4);
+                const float2 bq[NQ] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                                       make_float2(b1.z, b1.w)};
+                const float2 cq[NQ] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
+                                       make_float2(c1.z, c1.w)};
+                const float2 y2 = make_float2(yh, yh), d2 = make_float2(dl, dl), u2 = make_float2(uu, uu),
+                             du2 = make_float2(du, du);
+                float v[SPT];                          // dB partials of this lane's states
+                float2 sLB = make_float2(0.f, 0.f);    // Σ λ·B (first order) or Σ λ·φ·B (exact hold)
+                float2 sAB = make_float2(0.f, 0.f);    // Σ λ·Ā·B (exact hold)
+                float2 sAA = make_float2(0.f, 0.f);    // Σ λ·h_{t−1}·Ā·A
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    lam[q] = __ffma2_rn(cq[q], y2, lam[q]);            // λ_t: the read-out at t joins
+                    const float2 x = __fmul2_rn(d2, A2[q]);
+                    const float2 ab = make_float2(ex2(x.x), ex2(x.y));
+                    const float2 dabA = __fmul2_rn(__fmul2_rn(lam[q], hprev[q]), ab);  // ∂/∂Ā · Ā
+                    sAA = __ffma2_rn(dabA, Af[q], sAA);                // ∂Ā/∂Δ = A·Ā
+                    dA[q] = __ffma2_rn(dabA, d2, dA[q]);               // ∂Ā/∂A = Δ·Ā
+                    float2 db;
+                    if (ZOH) {
+                        const float2 xn = __fmul2_rn(x, make_float2(kLn2, kLn2));
+                        const float2 phi = make_float2(zoh_phi(xn.x, ab.x), zoh_phi(xn.y, ab.y));
+                        const float2 psi = make_float2(zoh_psi(xn.x, ab.x, phi.x), zoh_psi(xn.y, ab.y, phi.y));
+                        const float2 lb = __fmul2_rn(lam[q], bq[q]);
+                        sLB = __ffma2_rn(lb, phi, sLB);                // du: Σ λ·Δ·φ·B (Δ applied below)
+                        sAB = __ffma2_rn(lb, ab, sAB);                 // ∂B̄/∂Δ = Ā·B
+                        db = __fmul2_rn(__fmul2_rn(lam[q], du2), phi); // ∂B̄/∂B = Δ·φ
+                        // ∂B̄/∂A = B·Δ²·ψ(ΔA)
+                        dA[q] = __ffma2_rn(__fmul2_rn(__fmul2_rn(lb, u2), __fmul2_rn(d2, d2)), psi, dA[q]);
+                    } else {
+                        sLB = __ffma2_rn(lam[q], bq[q], sLB);
+                        db = __fmul2_rn(lam[q], du2);                  // ∂B̄/∂B = Δ
+                    }
+                    v[2 * q] = db.x;
+                    v[2 * q + 1] = db.y;
+                    lam[q] = __fmul2_rn(lam[q], ab);                   // on to ∂/∂h_{t−1}
+                }
+                float slb = sLB.x + sLB.y, saa = sAA.x + sAA.y, sab = sAB.x + sAB.y;
+                if (NG == 2) {
+                    slb += __shfl_xor_sync(FULL, slb, 1);
+                    saa += __shfl_xor_sync(FULL, saa, 1);
+                    if (ZOH) sab += __shfl_xor_sync(FULL, sab, 1);
+                }
+                const float dut = fmaf(yh, skip, dl * slb);
+                const float ddr = (ZOH ? fmaf(uu, sab, saa) : fmaf(uu, slb, saa)) * sm.Sg[e];
+                dD_acc = fmaf(yh, uu, dD_acc);
+                db_acc += ddr;
+                if (g == 0) {
+                    sm.Odu[e] = dut;
+                    sm.Odd[e] = ddr;
+                    if (HAS_Z) sm.Odz[e] = sm.Gp[e] * sm.Sp[e];
+                }
+                // dB: sum the lane's 8 partials over the warp's channels; each
+                // shuffle step halves what a lane holds, the rest add in full
+                constexpr int B0 = NG == 2 ? 1 : 0;     // first lane bit that selects a channel
+#pragma unroll
+                for (int s = 0; s < 3; ++s) {
+                    const int w = 4 >> s;
+                    const bool hb = (lane >> (B0 + s)) & 1;
+#pragma unroll
+                    for (int j = 0; j < w; ++j) {
+                        const float lo = v[j], hi = v[j + w];
+                        const float send = hb ? lo : hi, keep = hb ? hi : lo;
+                        v[j] = keep + __shfl_xor_sync(FULL, send, 1 << (B0 + s));
+                    }
+                }
+#pragma unroll
+                for (int bit = B0 + 3; bit < 5; ++bit) v[0] += __shfl_xor_sync(FULL, v[0], 1 << bit);
+                const int idx = (((lane >> B0) & 1) << 2) | (((lane >> (B0 + 1)) & 1) << 1) | ((lane >> (B0 + 2)) & 1);
+                if ((lane >> (B0 + 3)) == 0) sm.acc[(t * 2) * NP + SPT * g + idx] = v[0];
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) hcur[q] = hprev[q];
+            }
+            __syncwarp();
+
+            // ---- the tile's dB, dC channel sums into memory (lane: one token,
+            // one of dB / dC, every state); du, dΔraw, dz out
+            {
+                const int t = lane & 15, m = lane >> 4;
+                if (t0 + t < L) {
+                    float *dst = (m ? a.dC : a.dB) + (size_t)it.b * N * L + t0 + t;
+                    for (int n = 0; n < N; ++n) atomicAdd(dst + (size_t)n * L, sm.acc[(t * 2 + m) * NP + n]);
+                }
+            }
+            if (live) {
+                T *gdu = static_cast<T *>(a.du) + rowoff, *gdd = static_cast<T *>(a.ddelta) + rowoff;
+                T *gdz = HAS_Z && a.dz ? static_cast<T *>(a.dz) + rowoff : nullptr;
+#pragma unroll
+                for (int i = 0; i < OWN; ++i) {
+                    const int j = OWN * g + i, t = t0 + j;
+                    if (t < L) {
+                        gdu[t] = IO<T>::from_f(sm.Odu[c * TSP + j]);
+                        gdd[t] = IO<T>::from_f(sm.Odd[c * TSP + j]);
+                        if (gdz) gdz[t] = IO<T>::from_f(sm.Odz[c * TSP + j]);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+
+        // ---- item end: hand the adjoint on, or write dh0; add the sums
+        if (it.k > 0) {
+            if (live) {
+                float *dst = a.carry_rev + ((size_t)it.b * D + d) * N;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const int n = SPT * g + 2 * q;
+                    if (n < N) dst[n] = lam[q].x;
+                    if (n + 1 < N) dst[n + 1] = lam[q].y;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) st_release_b(a.flags_rev + it.grp, r + 1);
+        } else if (a.dh0 && live) {
+            float *dst = a.dh0 + ((size_t)it.b * D + d) * N;
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const int n = SPT * g + 2 * q;
+                if (n < N) dst[n] = lam[q].x;
+                if (n + 1 < N) dst[n + 1] = lam[q].y;
+            }
+        }
+        if (live) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const int n = SPT * g + 2 * q;
+                if (n < N) atomicAdd(a.dA + (size_t)d * N + n, dA[q].x);
+                if (n + 1 < N) atomicAdd(a.dA + (size_t)d * N + n + 1, dA[q].y);
+            }
+            if (g == 0) {
+                if (a.dDskip) atomicAdd(a.dDskip + d, dD_acc);
+                if (a.dbias) atomicAdd(a.dbias + d, db_acc);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+int resident_warps(const void *kern, size_t smem) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, smem) != cudaSuccess) return 0;
+    per_sm = std::max(1, std::min(per_sm, kBwdWarpsPerSM));
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return per_sm * sms;
+}
+
+template <typename T, int NG, bool HAS_Z, bool ZOH, bool VEC>
+cudaError_t launch_pair(const BwdArgs &a, cudaStream_t st) {
+    const int items = a.groups * a.nchunks;
+    auto k1 = bwd_ckpt_kernel<T, NG, ZOH, VEC>;
+    static int res1 = 0;
+    if (res1 == 0) res1 = resident_warps(reinterpret_cast<const void *>(k1), 0);
+    if (res1 == 0) return cudaErrorInvalidConfiguration;
+    k1<<<std::max(1, std::min(items, res1)), 32, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    auto k2 = bwd_rev_kernel<T, NG, HAS_Z, ZOH, VEC>;
+    constexpr size_t smem = sizeof(RevSmem<NG>);
+    static int res2 = 0;
+    if (res2 == 0) {
+        e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        res2 = resident_warps(reinterpret_cast<const void *>(k2), smem);
+    }
+    if (res2 == 0) return cudaErrorInvalidConfiguration;
+    k2<<<std::max(1, std::min(items, res2)), 32, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int NG>
+cudaError_t dispatch_bwd(const BwdArgs &a, bool vec, cudaStream_t st) {
+    const bool z = a.z != nullptr, zoh = a.zoh != 0;
+#define SSM_BWD_CASE(Z, H, V) \
+    if (z == Z && zoh == H && vec == V) return launch_pair<T, NG, Z, H, V>(a, st);
+    SSM_BWD_CASE(true, false, true)
+    SSM_BWD_CASE(true, false, false)
+    SSM_BWD_CASE(false, false, true)
+    SSM_BWD_CASE(false, false, false)
+    SSM_BWD_CASE(true, true, true)
+    SSM_BWD_CASE(true, true, false)
+    SSM_BWD_CASE(false, true, true)
+    SSM_BWD_CASE(false, true, false)
+#undef SSM_BWD_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int bwd_cpw(int64_t dstate) { return dstate <= 8 ? 32 : 16; }
+
+cudaError_t bwd_launch(const BwdArgs &a, bool bf16, cudaStream_t st) {
+    // 8-token vector loads need 16-byte rows: L a multiple of 8 and aligned bases
+    auto al16 = [](const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    const bool vec = a.seqlen % 8 == 0 && al16(a.u) && al16(a.delta) && al16(a.z) && al16(a.dy);
+    if (bf16) return a.dstate <= 8 ? dispatch_bwd<__nv_bfloat16, 1>(a, vec, st) : dispatch_bwd<__nv_bfloat16, 2>(a, vec, st);
+    return a.dstate <= 8 ? dispatch_bwd<float, 1>(a, vec, st) : dispatch_bwd<float, 2>(a, vec, st);
+}
+
+}  // namespace ssm

@@ -53,6 +53,26 @@ struct StepArgs {
     void *y;
 };
 
+// Backward scan: gradients of the forward scan for upstream dy (and dhL).
+struct BwdArgs {
+    int batch, dim, dstate, seqlen;
+    const void *u, *delta, *z, *B, *C, *dy;
+    const float *A, *Dskip, *bias, *h0, *dhL;
+    int delta_softplus;
+    int zoh;
+    void *du, *ddelta, *dz;          // b × D × L, I/O type (dz may be null)
+    float *dB, *dC;                  // b × N × L fp32, zeroed before the launches
+    float *dA;                       // D × N fp32, zeroed
+    float *dDskip, *dbias;           // D fp32 or null, zeroed
+    float *dh0;                      // b × D × N fp32 or null
+    int *status;                     // device status word
+    int *tickets;                    // two work counters (checkpoint pass, reverse pass)
+    int *flags_fwd, *flags_rev;      // chunks finished per channel group, per pass
+    float *carry_fwd, *carry_rev;    // b × D × N hand-offs: the state forward, the adjoint backward
+    float *ckpt;                     // [group][tile][2][32 lanes] float4: the state at every tile start
+    int chunk_len, nchunks, groups, ntiles;
+};
+
 // Causal depthwise convolution + bias + optional SiLU over whole sequences.
 struct ConvArgs {
     int64_t batch, dim, seqlen;
@@ -82,6 +102,10 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
 cudaError_t scan_launch(const ScanArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t step_launch(const StepArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t conv_launch(const ConvArgs &a, bool bf16, cudaStream_t stream);
+cudaError_t bwd_launch(const BwdArgs &a, bool bf16, cudaStream_t stream);
+int bwd_cpw(int64_t dstate);             // channels per warp of the backward kernels
+constexpr int kBwdTile = 16;             // tokens per checkpoint / recompute tile
+constexpr int kBwdChunk = 256;           // tokens per work item of the backward passes
 cudaError_t conv_step_launch(const ConvStepArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t mufu_ex2_launch(float *sink, int blocks, int iters, cudaStream_t stream);
 

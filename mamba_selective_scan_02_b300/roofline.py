@@ -48,6 +48,19 @@ def algorithmic_bytes_conv_step(batch: int, dim: int, width: int, io_bytes: int)
     return batch * dim * (2 * (width - 1) + 2) * io_bytes + dim * (width + 1) * 4
 
 
+def algorithmic_bytes_bwd(batch: int, dim: int, dstate: int, seqlen: int, io_bytes: int,
+                          has_z: bool = True) -> int:
+    """Bytes the backward scan must move at minimum: u, Δraw, (z,) dy read and
+    du, dΔraw, (dz) written once per (b, d, t); B, C read and dB, dC (fp32)
+    written once per (b, n, t); A, D, bias read and their fp32 gradients
+    written once.  The states are recomputed, never read from memory."""
+    per_elem = (4 if has_z else 3) + (3 if has_z else 2)
+    n = batch * dim * seqlen * per_elem * io_bytes
+    n += batch * dstate * seqlen * (2 * io_bytes + 2 * 4)
+    n += 2 * (dim * dstate * 4 + 2 * dim * 4)
+    return n
+
+
 def exps_scan(batch: int, dim: int, dstate: int, seqlen: int) -> int:
     """One exponential Ā = exp(Δ·A) per (b, d, n, t)."""
     return batch * dim * dstate * seqlen

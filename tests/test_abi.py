@@ -232,3 +232,49 @@ def test_conv_step_rejects_before_launch(over, code):
 def test_conv_null_params():
     assert capi.lib().ssm_conv1d_fwd(None, None) == capi.SSM_ERR_INVALID_ARG
     assert capi.lib().ssm_conv1d_step(None, None) == capi.SSM_ERR_INVALID_ARG
+
+
+def valid_bwd(**over):
+    p = capi.BwdParams()
+    p.batch, p.dim, p.dstate, p.seqlen = 2, 64, 16, 256
+    p.io_dtype = capi.SSM_BF16
+    step = 1 << 20
+    names = ["u", "delta", "z", "B", "C", "A", "Dskip", "delta_bias", "dy", "du", "ddelta", "dz",
+             "dB", "dC", "dA", "workspace"]
+    for i, n in enumerate(names):
+        setattr(p, n, FAKE + i * step)
+    p.delta_softplus = 1
+    p.workspace_bytes = 1 << 30
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(batch=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(dstate=17), capi.SSM_ERR_UNSUPPORTED),
+    (dict(io_dtype=5), capi.SSM_ERR_INVALID_ARG),
+    (dict(dy=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(dA=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(workspace=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(workspace_bytes=1024), capi.SSM_ERR_INVALID_ARG),
+    (dict(chunk_len=24), capi.SSM_ERR_INVALID_ARG),            # not a multiple of 16
+    (dict(u=FAKE + 1), capi.SSM_ERR_INVALID_ARG),               # bf16 at an odd address
+    (dict(dB=FAKE + 12 * (1 << 20) + 2), capi.SSM_ERR_INVALID_ARG),
+    (dict(workspace=FAKE + 15 * (1 << 20) + 4), capi.SSM_ERR_INVALID_ARG),  # not 16-byte aligned
+    (dict(du=FAKE + 64), capi.SSM_ERR_INVALID_ARG),             # du overlaps u
+    (dict(zoh=3), capi.SSM_ERR_INVALID_ARG),
+])
+def test_bwd_rejects_before_launch(over, code):
+    assert capi.ssm_scan_bwd(valid_bwd(**over), None) == code
+
+
+def test_bwd_workspace_size():
+    p = valid_bwd()
+    groups = 2 * 64 // 16
+    ntiles = 256 // 16
+    flags = -(-groups * 4 // 256) * 256
+    bdn = -(-2 * 64 * 16 * 4 // 256) * 256
+    assert capi.ssm_scan_bwd_workspace_size(p) == 256 + 2 * flags + 2 * bdn + groups * ntiles * 1024
+    assert capi.ssm_scan_bwd_workspace_size(valid_bwd(seqlen=0)) == 0
+    assert capi.lib().ssm_scan_bwd(None, None) == capi.SSM_ERR_INVALID_ARG
