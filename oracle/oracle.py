@@ -61,6 +61,9 @@ def _bind(lib):
                                     _D, _D, _D, _D, _D, _D, _D, _D,
                                     ctypes.c_int, ctypes.c_int, _D, _D, _D,
                                     _D, _D, _D, _D, _D, _D, _D, _D, _D, _I64, _I64]
+    lib.oracle_ssd.restype = ctypes.c_int
+    lib.oracle_ssd.argtypes = [_I64, _I64, _I64, _I64, _I64, _D, _D, _D, _D, _D, _D, _D,
+                               ctypes.c_int, _D, _D, _D]
     lib.oracle_step.restype = ctypes.c_int
     lib.oracle_step.argtypes = [_I64, _I64, _I64,
                                 _D, _D, _D, _D, _D, _D, _D, _D, _D,
@@ -228,3 +231,21 @@ def scan_bwd(u, delta, A, B, C, dy, Dskip=None, z=None, bias=None, h0=None, dhL=
     out = {k: sum(p[k] for p in parts) for k in parts[0]}
     out.update(du=du, ddelta=ddelta, dz=dz, dh0=dh0)
     return out
+
+
+def ssd(x, dt, A, B, C, Dskip=None, dt_bias=None, h0=None, dt_softplus=True, lib=None):
+    """Mamba-2 (SSD) forward.  x: (b, L, H, P); dt: (b, L, H); A, Dskip, dt_bias:
+    (H,); B, C: (b, L, N); h0: (b, H, P, N).  Returns (y (b, L, H, P), hL
+    (b, H, P, N)) in fp64."""
+    lib = lib or load()
+    x, dt, A, B, C, Dskip, dt_bias, h0 = map(_f64, (x, dt, A, B, C, Dskip, dt_bias, h0))
+    b, L, H, P = x.shape
+    N = B.shape[2]
+    assert dt.shape == (b, L, H) and B.shape == (b, L, N) and C.shape == (b, L, N) and A.shape == (H,)
+    y = np.empty((b, L, H, P))
+    hL = np.empty((b, H, P, N))
+    rc = lib.oracle_ssd(b, L, H, P, N, _p(x), _p(dt), _p(A), _p(B), _p(C), _p(Dskip), _p(dt_bias),
+                        int(bool(dt_softplus)), _p(h0), _p(y), _p(hL))
+    if rc != 0:
+        raise RuntimeError("oracle_ssd failed")
+    return y, hL

@@ -66,6 +66,14 @@
  * formulas, so this is calculus on the forward definition above, and it is
  * pinned to central finite differences of oracle_scan.
  *
+ * The Mamba-2 layer (oracle_ssd) restricts A_t to a scalar times the identity
+ * per head: a_t = exp(Δ_t A_h), heads of P channels share a_t, B_t and C_t, and
+ * each head's state is an N × P matrix [first-principles page — "Mamba-2:
+ * state space duality"]:
+ *   S_t = a_t S_{t−1} + Δ_t B_t x_tᵀ,   y_t = S_tᵀ C_t + D_h x_t.
+ * The chunked SSD algorithm on the same page reaches exactly this result (it
+ * reorders the same sums), so the oracle is the recurrence itself.
+ *
  * Parity is pinned by tests/test_oracle_pins.py (worked example, convolution
  * kernel, gated-RNN reduction, Δ limits, first output, product-form brute
  * force, continuation; for the short convolution: numpy's convolution, the
@@ -408,5 +416,58 @@ int oracle_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                 dh0[c * N + n] = lam[n];
     }
     free(h); free(dt); free(pre); free(lam);
+    return 0;
+}
+
+/*
+ * Mamba-2 (SSD) forward for every batch element and head.
+ *   x, y : batch × seqlen × nheads × headdim   (token-major, as the block's
+ *          projection produces them)
+ *   dt   : batch × seqlen × nheads             Δraw per head
+ *   B, C : batch × seqlen × dstate             one group shared by all heads
+ *   A, Dskip, dt_bias : nheads                 (Dskip, dt_bias may be NULL)
+ *   h0, hL : batch × nheads × headdim × dstate (NULL = zeros / not written)
+ * Δ = softplus(Δraw + dt_bias) when dt_softplus, else Δraw + dt_bias.
+ * Returns 0, or -1 on bad sizes or allocation failure.
+ */
+int oracle_ssd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+               const double *x, const double *dt, const double *A, const double *B,
+               const double *C, const double *Dskip, const double *dt_bias, int dt_softplus,
+               const double *h0, double *y, double *hL)
+{
+    if (headdim < 1 || dstate < 1)
+        return -1;
+    const int64_t P = headdim, N = dstate, H = nheads, L = seqlen;
+    double *S = (double *)malloc((size_t)P * N * sizeof(double));
+    if (!S)
+        return -1;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t h = 0; h < H; ++h) {
+            for (int64_t i = 0; i < P * N; ++i)
+                S[i] = h0 ? h0[(b * H + h) * P * N + i] : 0.0;
+            for (int64_t t = 0; t < L; ++t) {
+                double d = dt[(b * L + t) * H + h] + (dt_bias ? dt_bias[h] : 0.0);
+                if (dt_softplus)
+                    d = oracle_softplus(d);
+                const double a = exp(d * A[h]);
+                const double *xt = x + ((b * L + t) * H + h) * P;
+                const double *Bt = B + (b * L + t) * N;
+                const double *Ct = C + (b * L + t) * N;
+                double *yt = y + ((b * L + t) * H + h) * P;
+                for (int64_t p = 0; p < P; ++p) {
+                    double acc = 0.0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        S[p * N + n] = a * S[p * N + n] + d * Bt[n] * xt[p];
+                        acc += S[p * N + n] * Ct[n];
+                    }
+                    yt[p] = acc + (Dskip ? Dskip[h] : 0.0) * xt[p];
+                }
+            }
+            if (hL)
+                for (int64_t i = 0; i < P * N; ++i)
+                    hL[(b * H + h) * P * N + i] = S[i];
+        }
+    }
+    free(S);
     return 0;
 }

@@ -469,7 +469,88 @@ def pin_backward_finite_differences(lib, seed=21):
             _close(g[key], fd, 0, 1e-7 * (1 + np.abs(fd).max()), f"backward {key} {cs}")
 
 
+# --------------------------------------------------------------------------
+# P13: a Mamba-2 head is Mamba-1 with one A for every state (first-principles
+# page — "Mamba-2: state space duality": A_t is a scalar times the identity,
+# heads of P channels share a_t, B_t and C_t).  oracle_ssd must equal
+# oracle_scan run on the head's P channels with A[d, n] = A_h, Δraw of the head,
+# the shared B, C, no gate — an independent implementation of the recurrence.
+
+def pin_ssd_is_mamba1_with_scalar_A(lib, seed=22):
+    rng = np.random.default_rng(seed)
+    b, L, H, P, N = 2, 19, 3, 4, 5
+    x = rng.normal(size=(b, L, H, P))
+    dt = rng.normal(size=(b, L, H))
+    A = -rng.uniform(0.2, 2.0, H)
+    B = rng.normal(size=(b, L, N))
+    C = rng.normal(size=(b, L, N))
+    Dh = rng.normal(size=H)
+    bias = rng.normal(size=H)
+    h0 = rng.normal(size=(b, H, P, N))
+    for soft in (True, False):
+        dtu = dt if soft else np.abs(dt) + 0.05
+        y, hL = orc.ssd(x, dtu, A, B, C, Dskip=Dh, dt_bias=bias if soft else None, h0=h0,
+                        dt_softplus=soft, lib=lib)
+        u = x.transpose(0, 2, 3, 1).reshape(b, H * P, L)              # channel h·P + p
+        delta = np.repeat(dtu.transpose(0, 2, 1), P, axis=1)           # (b, H·P, L)
+        A1 = np.repeat(A, P)[:, None].repeat(N, axis=1)                # (H·P, N)
+        ym, hm = orc.scan(u, delta, A1, B.transpose(0, 2, 1), C.transpose(0, 2, 1), Dskip=np.repeat(Dh, P),
+                          bias=np.repeat(bias, P) if soft else None, h0=h0.reshape(b, H * P, N),
+                          delta_softplus=soft, lib=lib)
+        _close(y, ym.reshape(b, H, P, L).transpose(0, 3, 1, 2), 1e-12, 1e-13, "SSD = Mamba-1 with scalar A")
+        _close(hL, hm.reshape(b, H, P, N), 1e-12, 1e-13, "SSD final state")
+
+
+# P14: the duality — unrolled, the layer is one masked matrix product
+# Y = (L ∘ C Bᵀ)(Δ·X) + D X with L[i, j] = exp(Σ_{k=j+1..i} Δ_k A_h) for i >= j
+# (and 0 above the diagonal), plus the initial state read through the decay
+# from the start, exp(Σ_{k<=i} Δ_k A_h)·C_i·S_0 (same section: "the whole layer
+# is one matrix product", causal attention with a decay mask).
+
+def pin_ssd_matrix_form(lib, seed=23):
+    rng = np.random.default_rng(seed)
+    b, L, H, P, N = 2, 23, 2, 3, 6
+    x = rng.normal(size=(b, L, H, P))
+    dt = rng.normal(size=(b, L, H))
+    A = -rng.uniform(0.1, 1.5, H)
+    B = rng.normal(size=(b, L, N))
+    C = rng.normal(size=(b, L, N))
+    Dh = rng.normal(size=H)
+    bias = rng.normal(size=H)
+    h0 = rng.normal(size=(b, H, P, N))
+    y, _ = orc.ssd(x, dt, A, B, C, Dskip=Dh, dt_bias=bias, h0=h0, lib=lib)
+    want = np.zeros_like(y)
+    for bi in range(b):
+        for h in range(H):
+            delta = _softplus(dt[bi, :, h] + bias[h])
+            cs = np.cumsum(delta * A[h])
+            Lm = np.tril(np.exp(cs[:, None] - cs[None, :]))
+            G = C[bi] @ B[bi].T
+            want[bi, :, h, :] = (Lm * G) @ (delta[:, None] * x[bi, :, h, :])
+            want[bi, :, h, :] += np.exp(cs)[:, None] * (C[bi] @ h0[bi, h].T)
+            want[bi, :, h, :] += Dh[h] * x[bi, :, h, :]
+    _close(y, want, 1e-11, 1e-12, "SSD matrix form")
+
+
+# P15: the Mamba-2 2.7B shapes against the printed totals: 80 heads × 64 = 5,120
+# channels, an input projection 2·5120 + 2·128 + 80 wide (one B and C group,
+# one Δ per head), and 40,216,560 weights per layer with a width-4 convolution
+# over x, B, C (plus bias), per-head Δ bias, A and D, and a gated norm.
+
+def pin_mamba2_counts(lib):
+    g = {k: int(v[0]) for k, v in read_golden("mamba28b_counts.txt").items()}
+    dm, H, P, N, W = g["d_model"], g["m2_heads"], g["m2_headdim"], g["m2_dstate"], g["conv_width"]
+    E = H * P
+    assert E == g["inner"]
+    proj = 2 * E + 2 * N + H
+    assert proj == g["m2_in_proj_out"]
+    conv = (E + 2 * N) * (W + 1)
+    layer = dm * proj + conv + 3 * H + E + E * dm + dm
+    assert layer == g["m2_layer_weights"]
+
+
 ALL_PINS = [pin_worked_example, pin_lti_convolution, pin_gated_rnn, pin_delta_limits,
             pin_first_output, pin_product_form, pin_continuation, pin_decode_equals_scan,
             pin_conv_library, pin_conv_impulse, pin_conv_continuation, pin_block_counts,
-            pin_backward_finite_differences]
+            pin_backward_finite_differences, pin_ssd_is_mamba1_with_scalar_A, pin_ssd_matrix_form,
+            pin_mamba2_counts]

@@ -62,6 +62,15 @@ MUTANTS = {
                                "dB[b * N * L + n * L + t] += dbbar * dt[t];"),
     "bwd_no_decay_propagation": ("lam[n] *= abar;", "lam[n] *= 1.0;"),
     "bwd_dD_missing": ("dDskip[d] += yhat * u_c[t];", "dDskip[d] += 0.0;"),
+    "ssd_no_decay": ("S[p * N + n] = a * S[p * N + n] + d * Bt[n] * xt[p];",
+                     "S[p * N + n] = S[p * N + n] + d * Bt[n] * xt[p];"),
+    "ssd_input_without_delta": ("S[p * N + n] = a * S[p * N + n] + d * Bt[n] * xt[p];",
+                                "S[p * N + n] = a * S[p * N + n] + Bt[n] * xt[p];"),
+    "ssd_readout_with_B": ("acc += S[p * N + n] * Ct[n];", "acc += S[p * N + n] * Bt[n];"),
+    "ssd_skip_dropped": ("yt[p] = acc + (Dskip ? Dskip[h] : 0.0) * xt[p];", "yt[p] = acc;"),
+    "ssd_dt_bias_dropped": ("double d = dt[(b * L + t) * H + h] + (dt_bias ? dt_bias[h] : 0.0);",
+                            "double d = dt[(b * L + t) * H + h];"),
+    "ssd_A_of_head_0": ("const double a = exp(d * A[h]);", "const double a = exp(d * A[0]);"),
 }
 
 
