@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-conv", action="store_true", help="skip the convolution kernels")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward scan")
+    ap.add_argument("--no-ssd", action="store_true", help="skip the Mamba-2 (SSD) layer scan")
     ap.add_argument("--bwd-batch", type=int, default=0,
                     help="sequences of the layer the backward runs on (default: all of them)")
     ap.add_argument("--no-other", action="store_true", help="skip the other scan workloads")
@@ -548,6 +549,54 @@ def run_ours(args):
             "l2": "L2 flushed before every launch (256 MB written, 256 MB read)"}
         out["gpu_launches"] += 23 * 2
         del dy, bout, bws, bi
+
+    # ---- the Mamba-2 layer scan (SSD): the Mamba-2 2.7B layer (80 heads of 64,
+    # N = 128) at the same batch and length, L2 flushed before every launch
+    if not args.no_ssd:
+        from mamba_selective_scan_02_b300.inputs import make_ssd_inputs
+        from mamba_selective_scan_02_b300.roofline import algorithmic_bytes_ssd, flops_ssd
+        sb, sL, sH, sP, sN = w.batch, w.seqlen, 80, 64, 128
+        si = make_ssd_inputs(sb, sL, sH, sP, sN, seed=51, device=dev)
+        sy = torch.empty_like(si["x"])
+        shL = torch.empty((sb, sH, sP, sN), dtype=torch.float32, device=dev)
+        sp = api.ssd_params(si["x"], si["dt"], si["A"], si["B"], si["C"], si["D"], si["dt_bias"], None,
+                            y=sy, hL=shL)
+        for _ in range(3):
+            capi.check(capi.ssm_ssd_fwd(sp, sh), "ssm_ssd_fwd")
+        tms = []
+        for _ in range(30):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            capi.ssm_ssd_fwd(sp, sh)
+            e1.record(stream)
+            tms.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        sms_ = statistics.median(a_.elapsed_time(b_) for a_, b_ in tms)
+        sbytes = algorithmic_bytes_ssd(sb, sL, sH, sP, sN)
+        sflops = flops_ssd(sb, sL, sH, sP, sN)
+        sgbs = sbytes / (sms_ / 1e3) / 1e9
+        stf = sflops / (sms_ / 1e3) / 1e12
+        bf16_peak = None
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                bf16_peak = float(json.load(f)["bf16_tflops"])
+        except (OSError, ValueError, KeyError):
+            bf16_peak = 1800.0  # the profiling recipe's fallback burst figure
+        t_hbm, t_tc = sbytes / (hbm_peak * 1e9), (sflops / (bf16_peak * 1e12) if bf16_peak else 0.0)
+        bound = "hbm" if t_hbm >= t_tc else "tensor"
+        out["ssd"] = {
+            "workload": f"mamba2_2.7b_layer_b{sb}_L{sL}_H{sH}_P{sP}_N{sN}", "ms": sms_,
+            "value": sb * sL * sH * sP / (sms_ / 1e3) / 1e9, "unit": UNIT,
+            "roofline": ({"bound": "hbm", "achieved": sgbs, "peak": hbm_peak, "unit": "GB/s",
+                          "frac": sgbs / hbm_peak} if bound == "hbm" else
+                         {"bound": "tensor", "achieved": stf, "peak": bf16_peak, "unit": "TFLOP/s",
+                          "frac": stf / bf16_peak}),
+            "algorithmic_bytes": sbytes, "flops": sflops, "tflops": stf,
+            "tensor_path": "mma.sync m16n8k16 bf16 (fp32 accumulate)",
+            "l2": "L2 flushed before every launch (256 MB written, 256 MB read)"}
+        out["gpu_launches"] += 33
+        del si, sy, shL
 
     # ---- the short convolution in front of the scan: the layer shape (sequence
     # form) and the decode batch (one token), L2 flushed before every launch

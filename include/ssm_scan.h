@@ -188,6 +188,43 @@ size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params *p);
 ssm_status ssm_scan_bwd(const ssm_scan_bwd_params *p, ssm_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Mamba-2 layer scan (state space duality, SSD).
+ *
+ * Per batch b, head h (P channels, scalar A_h) and token t:
+ *   Δ_t   = softplus(dt[b,t,h] + dt_bias[h])   (or without softplus)
+ *   a_t   = exp(Δ_t · A[h])
+ *   S_t   = a_t · S_{t−1} + Δ_t · x_t ⊗ B_t     (S: P × N per head, S_{−1} = h0)
+ *   y_t   = S_t · C_t + Dskip[h] · x_t
+ * Source: "Mamba and selective state spaces, from first principles", section
+ * "Mamba-2: state space duality" (A a scalar times the identity per head,
+ * heads of P channels sharing a_t, B_t, C_t; the chunked algorithm that turns
+ * the layer into tensor-core products).  One group of B, C for all heads, as
+ * in the Mamba-2 2.7B projection the section describes.
+ *
+ * This build supports headdim P = 64, dstate N = 128 and bf16 I/O
+ * (SSM_ERR_UNSUPPORTED otherwise); the products take bf16 operands with fp32
+ * accumulation, the carried state is fp32.  Pointers are device pointers;
+ * x, B, C and y 16-byte aligned, the rest aligned to their element size.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int64_t batch, seqlen, nheads;   /* b, L, H */
+    int64_t headdim, dstate;         /* P (64), N (128) */
+    ssm_dtype io_dtype;              /* SSM_BF16 */
+    const void *x;                   /* b × L × H × P */
+    const void *dt;                  /* b × L × H: Δraw per head */
+    const float *A;                  /* H: the head's scalar A (negative for a decay) */
+    const void *B, *C;               /* b × L × N */
+    const float *Dskip, *dt_bias;    /* H fp32; NULL = 0 */
+    int dt_softplus;                 /* 1: Δ = softplus(dt + dt_bias); 0: Δ = dt + dt_bias */
+    const float *h0;                 /* b × H × P × N fp32; NULL = zeros */
+    void *y;                         /* out: b × L × H × P */
+    float *hL;                       /* out: b × H × P × N fp32; NULL = not written */
+} ssm_ssd_params;
+
+/* The Mamba-2 layer scan; one launch, no workspace. */
+ssm_status ssm_ssd_fwd(const ssm_ssd_params *p, ssm_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The short convolution in front of the SSM.
  *
  * Operation, per batch b, channel d and token t (W = width):

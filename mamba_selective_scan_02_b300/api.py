@@ -223,6 +223,50 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, h0=None, dh
     return out
 
 
+def ssd_params(x, dt, A, B, C, D=None, dt_bias=None, h0=None, *, y, hL=None,
+               dt_softplus=True) -> capi.SsdParams:
+    """Validate tensors and build the Mamba-2 scan's C parameter struct."""
+    if x.dtype not in _DT:
+        raise ValueError(f"unsupported I/O dtype {x.dtype}")
+    dev = x.device
+    b, L, H, P = x.shape
+    N = B.shape[2]
+    io = x.dtype
+    f32 = torch.float32
+    _need(x, "x", (b, L, H, P), io, dev)
+    _need(dt, "dt", (b, L, H), io, dev)
+    _need(A, "A", (H,), f32, dev)
+    _need(B, "B", (b, L, N), io, dev)
+    _need(C, "C", (b, L, N), io, dev)
+    _opt(D, "D", (H,), f32, dev)
+    _opt(dt_bias, "dt_bias", (H,), f32, dev)
+    _opt(h0, "h0", (b, H, P, N), f32, dev)
+    _need(y, "y", (b, L, H, P), io, dev)
+    _opt(hL, "hL", (b, H, P, N), f32, dev)
+    p = capi.SsdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate = b, L, H, P, N
+    p.io_dtype = _DT[io]
+    p.x, p.dt, p.A, p.B, p.C = _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C)
+    p.Dskip, p.dt_bias, p.dt_softplus = _ptr(D), _ptr(dt_bias), int(bool(dt_softplus))
+    p.h0, p.y, p.hL = _ptr(h0), _ptr(y), _ptr(hL)
+    return p
+
+
+def ssd_fwd(x, dt, A, B, C, D=None, dt_bias=None, h0=None, *, dt_softplus=True, y=None, hL=None,
+            return_last_state=True, stream=None):
+    """Mamba-2 layer scan: x (b, L, H, P), dt (b, L, H), A (H,), B, C (b, L, N).
+    Returns (y (b, L, H, P), hL (b, H, P, N) fp32 or None)."""
+    if y is None:
+        y = torch.empty_like(x)
+    if hL is None and return_last_state:
+        b, L, H, P = x.shape
+        hL = torch.empty((b, H, P, B.shape[2]), dtype=torch.float32, device=x.device)
+    p = ssd_params(x, dt, A, B, C, D, dt_bias, h0, y=y, hL=hL, dt_softplus=dt_softplus)
+    st = torch.cuda.current_stream(x.device).cuda_stream if stream is None else stream
+    capi.check(capi.ssm_ssd_fwd(p, st), "ssm_ssd_fwd")
+    return y, hL
+
+
 def conv_params(x, weight, bias=None, state_in=None, *, u, state_out=None, silu=True) -> capi.ConvParams:
     """Validate tensors and build the convolution's C parameter struct."""
     if x.dtype not in _DT:

@@ -62,6 +62,16 @@ class BwdParams(ctypes.Structure):
     ]
 
 
+class SsdParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("seqlen", _i64), ("nheads", _i64), ("headdim", _i64), ("dstate", _i64),
+        ("io_dtype", ctypes.c_int),
+        ("x", _vp), ("dt", _vp), ("A", _vp), ("B", _vp), ("C", _vp),
+        ("Dskip", _vp), ("dt_bias", _vp), ("dt_softplus", ctypes.c_int),
+        ("h0", _vp), ("y", _vp), ("hL", _vp),
+    ]
+
+
 class ConvParams(ctypes.Structure):
     _fields_ = [
         ("batch", _i64), ("dim", _i64), ("seqlen", _i64), ("width", _i64),
@@ -115,6 +125,8 @@ def lib():
             L.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(BwdParams)]
             L.ssm_scan_bwd.restype = ctypes.c_int
             L.ssm_scan_bwd.argtypes = [ctypes.POINTER(BwdParams), _vp]
+            L.ssm_ssd_fwd.restype = ctypes.c_int
+            L.ssm_ssd_fwd.argtypes = [ctypes.POINTER(SsdParams), _vp]
             L.ssm_conv1d_fwd.restype = ctypes.c_int
             L.ssm_conv1d_fwd.argtypes = [ctypes.POINTER(ConvParams), _vp]
             L.ssm_conv1d_step.restype = ctypes.c_int
@@ -175,6 +187,10 @@ def ssm_scan_bwd_workspace_size(p: BwdParams) -> int:
 
 def ssm_scan_bwd(p: BwdParams, stream: int) -> int:
     return lib().ssm_scan_bwd(ctypes.byref(p), stream)
+
+
+def ssm_ssd_fwd(p: SsdParams, stream: int) -> int:
+    return lib().ssm_ssd_fwd(ctypes.byref(p), stream)
 
 
 def ssm_conv1d_fwd(p: ConvParams, stream: int) -> int:

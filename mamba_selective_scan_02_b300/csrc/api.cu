@@ -317,6 +317,44 @@ ssm_status ssm_state_update(const ssm_step_params *p, ssm_stream_t stream) {
                : SSM_ERR_CUDA;
 }
 
+ssm_status ssm_ssd_fwd(const ssm_ssd_params *p, ssm_stream_t stream) {
+    if (!p) return SSM_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->seqlen < 1 || p->nheads < 1 || p->headdim < 1 || p->dstate < 1) return SSM_ERR_INVALID_ARG;
+    if (p->io_dtype != SSM_F32 && p->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (p->dt_softplus != 0 && p->dt_softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (!p->x || !p->dt || !p->A || !p->B || !p->C || !p->y) return SSM_ERR_INVALID_ARG;
+    if (p->io_dtype != SSM_BF16 || !ssm::ssd_supported(p->headdim, p->dstate)) return SSM_ERR_UNSUPPORTED;
+    if (p->batch * p->nheads > INT32_MAX / 2 || p->seqlen > INT32_MAX / 2) return SSM_ERR_UNSUPPORTED;
+    const void *a16[] = {p->x, p->B, p->C, p->y};
+    for (const void *q : a16)
+        if (!aligned16(q)) return SSM_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(p->dt) % 2 != 0) return SSM_ERR_INVALID_ARG;
+    const void *a4[] = {p->A, p->Dskip, p->dt_bias, p->h0, p->hL};
+    for (const void *q : a4)
+        if (q && !aligned4(q)) return SSM_ERR_INVALID_ARG;
+    const size_t seq = (size_t)p->batch * p->seqlen * p->nheads * p->headdim * 2;
+    const size_t bc = (size_t)p->batch * p->seqlen * p->dstate * 2;
+    if (overlaps(p->y, seq, p->x, seq) || overlaps(p->y, seq, p->B, bc) || overlaps(p->y, seq, p->C, bc) ||
+        overlaps(p->y, seq, p->dt, (size_t)p->batch * p->seqlen * p->nheads * 2))
+        return SSM_ERR_INVALID_ARG;
+    ssm::SsdArgs a;
+    a.batch = (int)p->batch;
+    a.seqlen = (int)p->seqlen;
+    a.nheads = (int)p->nheads;
+    a.x = p->x;
+    a.dt = p->dt;
+    a.B = p->B;
+    a.C = p->C;
+    a.A = p->A;
+    a.Dskip = p->Dskip;
+    a.dt_bias = p->dt_bias;
+    a.dt_softplus = p->dt_softplus;
+    a.h0 = p->h0;
+    a.y = p->y;
+    a.hL = p->hL;
+    return ssm::ssd_launch(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 ssm_status ssm_conv1d_fwd(const ssm_conv_params *p, ssm_stream_t stream) {
     if (!p) return SSM_ERR_INVALID_ARG;
     if (p->batch < 1 || p->dim < 1 || p->seqlen < 1) return SSM_ERR_INVALID_ARG;

@@ -73,6 +73,17 @@ struct BwdArgs {
     int chunk_len, nchunks, groups, ntiles;
 };
 
+// Mamba-2 (SSD) layer: heads of P channels with a scalar A each.
+struct SsdArgs {
+    int batch, seqlen, nheads;
+    const void *x, *dt, *B, *C;      // x: b × L × H × P; dt: b × L × H; B, C: b × L × N (bf16)
+    const float *A, *Dskip, *dt_bias;
+    int dt_softplus;
+    const float *h0;                 // b × H × P × N fp32 or null
+    void *y;                         // b × L × H × P
+    float *hL;                       // b × H × P × N fp32 or null
+};
+
 // Causal depthwise convolution + bias + optional SiLU over whole sequences.
 struct ConvArgs {
     int64_t batch, dim, seqlen;
@@ -102,6 +113,8 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
 cudaError_t scan_launch(const ScanArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t step_launch(const StepArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t conv_launch(const ConvArgs &a, bool bf16, cudaStream_t stream);
+bool ssd_supported(int64_t headdim, int64_t dstate);
+cudaError_t ssd_launch(const SsdArgs &a, cudaStream_t stream);
 cudaError_t bwd_launch(const BwdArgs &a, bool bf16, cudaStream_t stream);
 int bwd_cpw(int64_t dstate);             // channels per warp of the backward kernels
 constexpr int kBwdTile = 16;             // tokens per checkpoint / recompute tile

@@ -148,4 +148,31 @@ def make_conv_inputs(batch: int, dim: int, seqlen: int, width: int = 4, io_dtype
     return dict(x=x, weight=weight, bias=bias, state=state)
 
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "make_conv_inputs", "s4d_real_A", "torch_dtype"]
+def make_ssd_inputs(batch: int, seqlen: int, nheads: int = 80, headdim: int = 64, dstate: int = 128,
+                    seed: int = 0, device="cpu", with_h0: bool = False) -> dict:
+    """Seeded bf16 inputs for the Mamba-2 layer scan, shaped like the Mamba-2
+    2.7B layer of "Mamba-2: state space duality" (80 heads of 64, N = 128, one
+    B/C group).  x, B, C ~ N(0,1); dt ~ N(0, 0.5) with dt_bias =
+    log(expm1(U[1e-3, 1e-1])) per head (as the Mamba-1 workloads' Δ); A_h =
+    -U[1, 16] per head (Mamba-2 initialises A_log = log U[1, 16]); D ~ N(0,1);
+    h0 ~ N(0, 0.1) when asked.  Draw order: x, dt, B, C, A, D, dt_bias, h0."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    bf = torch.bfloat16
+    x = torch.randn((batch, seqlen, nheads, headdim), generator=g, device=device).to(bf)
+    dt = (torch.randn((batch, seqlen, nheads), generator=g, device=device) * 0.5).to(bf)
+    B = torch.randn((batch, seqlen, dstate), generator=g, device=device).to(bf)
+    C = torch.randn((batch, seqlen, dstate), generator=g, device=device).to(bf)
+    A = -(torch.rand(nheads, generator=g, device=device) * 15 + 1)
+    D = torch.randn(nheads, generator=g, device=device)
+    U = torch.empty(nheads, dtype=torch.float64, device=device)
+    U.uniform_(1e-3, 1e-1, generator=g)
+    dt_bias = torch.log(torch.expm1(U)).float()
+    h0 = None
+    if with_h0:
+        h0 = torch.randn((batch, nheads, headdim, dstate), generator=g, device=device) * 0.1
+    return dict(x=x, dt=dt, A=A, B=B, C=C, D=D, dt_bias=dt_bias, h0=h0)
+
+
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "make_conv_inputs", "make_ssd_inputs", "s4d_real_A",
+           "torch_dtype"]

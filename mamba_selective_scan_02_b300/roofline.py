@@ -61,6 +61,28 @@ def algorithmic_bytes_bwd(batch: int, dim: int, dstate: int, seqlen: int, io_byt
     return n
 
 
+def algorithmic_bytes_ssd(batch: int, seqlen: int, nheads: int, headdim: int, dstate: int,
+                          io_bytes: int = 2, has_hL: bool = True) -> int:
+    """Bytes the Mamba-2 layer scan must move: x read and y written once per
+    (b, t, h, p); B and C read once per (b, t, n) (one group for all heads); Δraw
+    once per (b, t, h); A, D, Δ bias once; the final state once."""
+    n = 2 * batch * seqlen * nheads * headdim * io_bytes
+    n += 2 * batch * seqlen * dstate * io_bytes + batch * seqlen * nheads * io_bytes
+    n += 3 * nheads * 4
+    n += batch * nheads * headdim * dstate * 4 * int(has_hL)
+    return n
+
+
+def flops_ssd(batch: int, seqlen: int, nheads: int, headdim: int, dstate: int, chunk: int = 64) -> int:
+    """Multiply-add FLOPs of the chunked SSD algorithm at chunk length Q: per
+    chunk and head, the causal half of C·Bᵀ (Q²·N) and of its product with X
+    (Q²·P), the inherited state's read-out C·Sᵀ (2·Q·N·P) and the chunk's state
+    Xᵀ·B (2·Q·N·P)."""
+    nch = -(-seqlen // chunk)
+    per = chunk * chunk * dstate + chunk * chunk * headdim + 4 * chunk * dstate * headdim
+    return batch * nheads * nch * per
+
+
 def exps_scan(batch: int, dim: int, dstate: int, seqlen: int) -> int:
     """One exponential Ā = exp(Δ·A) per (b, d, n, t)."""
     return batch * dim * dstate * seqlen

@@ -278,3 +278,35 @@ def test_bwd_workspace_size():
     assert capi.ssm_scan_bwd_workspace_size(p) == 256 + 2 * flags + 2 * bdn + groups * ntiles * 1024
     assert capi.ssm_scan_bwd_workspace_size(valid_bwd(seqlen=0)) == 0
     assert capi.lib().ssm_scan_bwd(None, None) == capi.SSM_ERR_INVALID_ARG
+
+
+def valid_ssd(**over):
+    p = capi.SsdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate = 2, 256, 4, 64, 128
+    p.io_dtype = capi.SSM_BF16
+    step = 1 << 22
+    for i, n in enumerate(["x", "dt", "A", "B", "C", "Dskip", "dt_bias", "y"]):
+        setattr(p, n, FAKE + i * step)
+    p.dt_softplus = 1
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(batch=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(nheads=0), capi.SSM_ERR_INVALID_ARG),
+    (dict(headdim=32), capi.SSM_ERR_UNSUPPORTED),
+    (dict(dstate=64), capi.SSM_ERR_UNSUPPORTED),
+    (dict(io_dtype=capi.SSM_F32), capi.SSM_ERR_UNSUPPORTED),
+    (dict(io_dtype=4), capi.SSM_ERR_INVALID_ARG),
+    (dict(x=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(A=None), capi.SSM_ERR_INVALID_ARG),
+    (dict(x=FAKE + 8), capi.SSM_ERR_INVALID_ARG),                # not 16-byte aligned
+    (dict(dt=FAKE + (1 << 22) + 1), capi.SSM_ERR_INVALID_ARG),
+    (dict(y=FAKE + 4096), capi.SSM_ERR_INVALID_ARG),             # y overlaps x
+    (dict(dt_softplus=2), capi.SSM_ERR_INVALID_ARG),
+])
+def test_ssd_rejects_before_launch(over, code):
+    assert capi.ssm_ssd_fwd(valid_ssd(**over), None) == code
+    assert capi.lib().ssm_ssd_fwd(None, None) == capi.SSM_ERR_INVALID_ARG
