@@ -97,6 +97,7 @@ KERNEL_SOURCES = {
     "conv1d_stream_kernel": ["conv1d.cu", "ssm_device.cuh", "ssm_internal.h"],
     "conv1d_step8_kernel": ["conv1d.cu", "ssm_device.cuh", "ssm_internal.h"],
     "bwd_rev_kernel": ["scan_bwd.cu", "ssm_device.cuh", "ssm_internal.h"],
+    "ssd_kernel": ["ssd.cu", "ssm_device.cuh", "ssm_internal.h"],
 }
 
 
@@ -589,7 +590,7 @@ def run_ours(args):
             "workload": f"mamba2_2.7b_layer_b{sb}_L{sL}_H{sH}_P{sP}_N{sN}", "ms": sms_,
             "value": sb * sL * sH * sP / (sms_ / 1e3) / 1e9, "unit": UNIT,
             "roofline": ({"bound": "hbm", "achieved": sgbs, "peak": hbm_peak, "unit": "GB/s",
-                          "frac": sgbs / hbm_peak} if bound == "hbm" else
+                          "frac": sgbs / hbm_peak, "traffic": recorded_traffic("ssd_kernel")} if bound == "hbm" else
                          {"bound": "tensor", "achieved": stf, "peak": bf16_peak, "unit": "TFLOP/s",
                           "frac": stf / bf16_peak}),
             "algorithmic_bytes": sbytes, "flops": sflops, "tflops": stf,
