@@ -19,10 +19,14 @@
 // operands that are not inputs — the inherited state, the decay-masked C·Bᵀ
 // block and the weighted B — enter as a pair of bf16 values (the rounded value
 // and the rounded remainder) and are multiplied twice, so they carry ~16 bits
-// instead of bf16's 8 whatever the input range.
+// instead of bf16's 8 whatever the input range.  The weighted B's remainder
+// lives in the C tile, free by then.
 //
 // One CTA of four warps owns one (sequence, head) and walks its chunks in
 // order; warp w owns rows 16w .. 16w+15 of the chunk's outputs and of the state.
+// Shared tiles are unpadded, with the 16-byte chunks of row r stored at chunk
+// position c ^ (r & 7), so the eight rows an ldmatrix reads hit eight
+// different bank groups; three CTAs fit on an SM.
 // Shapes built: P = 64, N = 128, bf16 I/O.
 #include <algorithm>
 
@@ -35,17 +39,21 @@ namespace {
 constexpr int Q = 64;                  // tokens per chunk
 constexpr int P = 64;                  // head dimension
 constexpr int NS = 128;                // state size
-constexpr int XS = P + 8;              // padded row (bf16 elements) of the x tile
-constexpr int BS = NS + 8;             // padded row of the B, C and state tiles
+constexpr int XS = P;                  // row (bf16 elements) of the x tile
+constexpr int BS = NS;                 // row of the B, C and state tiles
 constexpr int kThreads = 128;
+
+// Element (row, col) of a swizzled tile with `stride` elements per row.
+__device__ __forceinline__ int swz(int row, int col, int stride) {
+    return row * stride + ((((col >> 3) ^ (row & 7))) << 3) + (col & 7);
+}
 
 struct __align__(16) SsdSmem {
     __nv_bfloat16 x[Q * XS];           // x chunk, [token][p]
     __nv_bfloat16 B[Q * BS];           // B chunk, [token][n] (scaled by w_j for the state product)
-    __nv_bfloat16 C[Q * BS];           // C chunk, [token][n]
+    __nv_bfloat16 C[Q * BS];           // C chunk, [token][n]; then the weighted B's remainder
     __nv_bfloat16 S[P * BS];           // inherited state, [p][n]: bf16 value ...
     __nv_bfloat16 Sl[P * BS];          // ... and bf16 remainder
-    __nv_bfloat16 Bl[Q * BS];          // remainder of the weighted B
     float cum[Q], delta[Q], wsc[Q];    // prefix sums of Δ·A, Δ, and the state weights w_j
 };
 
@@ -83,26 +91,26 @@ __device__ __forceinline__ void mma16816(float *d, const uint32_t *a, uint32_t b
 // A fragment (16 × 16) of a row-major tile: rows r0.., columns k0.. (stride in elements).
 __device__ __forceinline__ void frag_a(uint32_t *a, const __nv_bfloat16 *base, int stride, int r0, int k0, int lane) {
     const int m = lane >> 3, r = lane & 7;
-    ldsm_x4(a, base + (r0 + r + 8 * (m & 1)) * stride + k0 + 8 * (m >> 1));
+    ldsm_x4(a, base + swz(r0 + r + 8 * (m & 1), k0 + 8 * (m >> 1), stride));
 }
 // A fragment of the transpose of a row-major tile: A[m][k] = tile[k][m].
 __device__ __forceinline__ void frag_a_t(uint32_t *a, const __nv_bfloat16 *base, int stride, int m0, int k0, int lane) {
     const int mi = lane >> 3, r = lane & 7;
-    ldsm_x4_t(a, base + (k0 + r + 8 * (mi >> 1)) * stride + m0 + 8 * (mi & 1));
+    ldsm_x4_t(a, base + swz(k0 + r + 8 * (mi >> 1), m0 + 8 * (mi & 1), stride));
 }
 // B fragments of two adjacent n-tiles (n0, n0 + 8) for one k-step, from a tile
 // stored [n][k] (k contiguous): b[0..1] for n-tile n0, b[2..3] for n0 + 8.
 __device__ __forceinline__ void frag_b_nk(uint32_t *b, const __nv_bfloat16 *base, int stride, int n0, int k0, int lane) {
     const int m = lane >> 3, r = lane & 7;
-    ldsm_x4(b, base + (n0 + r + 8 * (m >> 1)) * stride + k0 + 8 * (m & 1));
+    ldsm_x4(b, base + swz(n0 + r + 8 * (m >> 1), k0 + 8 * (m & 1), stride));
 }
 // The same from a tile stored [k][n] (n contiguous).
 __device__ __forceinline__ void frag_b_kn(uint32_t *b, const __nv_bfloat16 *base, int stride, int n0, int k0, int lane) {
     const int m = lane >> 3, r = lane & 7;
-    ldsm_x4_t(b, base + (k0 + r + 8 * (m & 1)) * stride + n0 + 8 * (m >> 1));
+    ldsm_x4_t(b, base + swz(k0 + r + 8 * (m & 1), n0 + 8 * (m >> 1), stride));
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 ssd_kernel(const SsdArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SsdSmem &sm = *reinterpret_cast<SsdSmem *>(smem_raw);
@@ -138,11 +146,11 @@ ssd_kernel(const SsdArgs a) {
             const int n = 8 * nt + 2 * tig;
             uint32_t hi, lo;
             split_bf16(Sacc[nt][0], Sacc[nt][1], hi, lo);
-            *reinterpret_cast<uint32_t *>(sm.S + (16 * w + gid) * BS + n) = hi;
-            *reinterpret_cast<uint32_t *>(sm.Sl + (16 * w + gid) * BS + n) = lo;
+            *reinterpret_cast<uint32_t *>(sm.S + swz(16 * w + gid, n, BS)) = hi;
+            *reinterpret_cast<uint32_t *>(sm.Sl + swz(16 * w + gid, n, BS)) = lo;
             split_bf16(Sacc[nt][2], Sacc[nt][3], hi, lo);
-            *reinterpret_cast<uint32_t *>(sm.S + (16 * w + gid + 8) * BS + n) = hi;
-            *reinterpret_cast<uint32_t *>(sm.Sl + (16 * w + gid + 8) * BS + n) = lo;
+            *reinterpret_cast<uint32_t *>(sm.S + swz(16 * w + gid + 8, n, BS)) = hi;
+            *reinterpret_cast<uint32_t *>(sm.Sl + swz(16 * w + gid + 8, n, BS)) = lo;
         }
     };
     store_state();
@@ -156,7 +164,7 @@ ssd_kernel(const SsdArgs a) {
             const int r = i / (P / 8), q = i % (P / 8), t = t0 + r;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (t < L) v = __ldg(reinterpret_cast<const uint4 *>(xg + (((size_t)b * L + t) * H + h) * P) + q);
-            *reinterpret_cast<uint4 *>(sm.x + r * XS + 8 * q) = v;
+            *reinterpret_cast<uint4 *>(sm.x + swz(r, 8 * q, XS)) = v;
         }
 #pragma unroll
         for (int i = tid; i < Q * (NS / 8); i += kThreads) {
@@ -166,8 +174,8 @@ ssd_kernel(const SsdArgs a) {
                 vb = __ldg(reinterpret_cast<const uint4 *>(Bg + ((size_t)b * L + t) * NS) + q);
                 vc = __ldg(reinterpret_cast<const uint4 *>(Cg + ((size_t)b * L + t) * NS) + q);
             }
-            *reinterpret_cast<uint4 *>(sm.B + r * BS + 8 * q) = vb;
-            *reinterpret_cast<uint4 *>(sm.C + r * BS + 8 * q) = vc;
+            *reinterpret_cast<uint4 *>(sm.B + swz(r, 8 * q, BS)) = vb;
+            *reinterpret_cast<uint4 *>(sm.C + swz(r, 8 * q, BS)) = vc;
         }
         if (w < 2) {
             const int i = tid, t = t0 + i;
@@ -281,7 +289,7 @@ ssd_kernel(const SsdArgs a) {
             for (int hr = 0; hr < 2; ++hr) {
                 const int i = r0 + gid + 8 * hr, t = t0 + i, p = 8 * nt + 2 * tig;
                 if (t < L) {
-                    const __nv_bfloat162 xv = *reinterpret_cast<const __nv_bfloat162 *>(sm.x + i * XS + p);
+                    const __nv_bfloat162 xv = *reinterpret_cast<const __nv_bfloat162 *>(sm.x + swz(i, p, XS));
                     const float y0 = fmaf(Dh, __low2float(xv), Y[nt][2 * hr]);
                     const float y1 = fmaf(Dh, __high2float(xv), Y[nt][2 * hr + 1]);
                     *reinterpret_cast<uint32_t *>(yg + (((size_t)b * L + t) * H + h) * P + p) = pack_bf16(y0, y1);
@@ -300,7 +308,7 @@ ssd_kernel(const SsdArgs a) {
             uint32_t hi, lo;
             split_bf16(f.x * wj, f.y * wj, hi, lo);
             *pb = hi;
-            reinterpret_cast<uint32_t *>(sm.Bl + r * BS)[q] = lo;
+            reinterpret_cast<uint32_t *>(sm.C + r * BS)[q] = lo;   // same swizzled position as in B
         }
         __syncthreads();
         {
@@ -320,7 +328,7 @@ ssd_kernel(const SsdArgs a) {
                 for (int np = 0; np < NS / 16; ++np) {
                     uint32_t bf[4], bl[4];
                     frag_b_kn(bf, sm.B, BS, 16 * np, 16 * ks, lane);
-                    frag_b_kn(bl, sm.Bl, BS, 16 * np, 16 * ks, lane);
+                    frag_b_kn(bl, sm.C, BS, 16 * np, 16 * ks, lane);
                     mma16816(Sacc[2 * np], af, bf[0], bf[1]);
                     mma16816(Sacc[2 * np + 1], af, bf[2], bf[3]);
                     mma16816(Sacc[2 * np], af, bl[0], bl[1]);
