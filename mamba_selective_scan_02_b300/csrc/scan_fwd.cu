@@ -12,7 +12,7 @@
 // this part the FP32 pipe and the MUFU are both busy at the same rate, and a
 // scheduler needs at least two resident warps to keep them fed, so:
 //   * A warp owns a group of CPW channels; NG = 1 or 2 lanes share a channel
-//     and each lane keeps SPT of its states in registers (packed f32x2 math,
+//     and each lane keeps SPT of its states in registers (scalar fp32 math,
 //     Ā = ex2.approx of Δ·A·log2e) while walking the time axis in order.
 //     With two lanes per channel the per-token partial sums C·h are combined
 //     with a transposed shuffle over four tokens.
@@ -48,6 +48,45 @@ namespace ssm {
 #ifndef SSM_SCAN_WARPS_PER_SM
 #define SSM_SCAN_WARPS_PER_SM 8
 #endif
+
+#ifndef SSM_SCAN_PACKED
+#define SSM_SCAN_PACKED 1
+#endif
+#ifndef SSM_SCAN_SCALAR_X
+#define SSM_SCAN_SCALAR_X 0
+#endif
+#ifndef SSM_SCAN_SCALAR_H
+#define SSM_SCAN_SCALAR_H 0
+#endif
+
+// Pairwise fp32 arithmetic of the recurrence, packed f32x2 by default.  A
+// microbenchmark of the bare update alone (Δ·A, ex2, B·Δu, Ā·h + B̄u, C·h, no
+// loads) retires 5.2 T updates/s with scalar FFMA/FMUL against 4.0 T packed at
+// 8 warps per SM, but in the whole kernel, where issue slots are the limit, the
+// scalar form's extra instructions cost more (290.6 µs against 262 µs on the
+// 4 × 5120 × 2048 layer).  SSM_SCAN_SCALAR_X / _H make only the product that
+// feeds the exponential, or the state update, scalar.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+#if SSM_SCAN_PACKED
+    return __fmul2_rn(a, b);
+#else
+    return make_float2(a.x * b.x, a.y * b.y);
+#endif
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+#if SSM_SCAN_PACKED
+    return __ffma2_rn(a, b, c);
+#else
+    return make_float2(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y));
+#endif
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+#if SSM_SCAN_PACKED
+    return __fadd2_rn(a, b);
+#else
+    return make_float2(a.x + b.x, a.y + b.y);
+#endif
+}
 
 constexpr int kTT = 32;                // tokens per tile (chunks are multiples of 64)
 constexpr int kWarpsPerSM = SSM_SCAN_WARPS_PER_SM;  // resident warps targeted per SM
@@ -337,14 +376,14 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 float2 odl[OP], odu[OP];
 #pragma unroll
                 for (int j = 0; j < OP; ++j) {
-                    float2 x = __fadd2_rn(make_float2(df[2 * j], df[2 * j + 1]), make_float2(bias, bias));
+                    float2 x = add2(make_float2(df[2 * j], df[2 * j + 1]), make_float2(bias, bias));
                     if (a.delta_softplus) x = make_float2(IO<T>::softplus(x.x), IO<T>::softplus(x.y));
                     if (valid < OWN) {  // Δ = 0 keeps the state: Ā = 1, B̄u = 0
                         if (2 * j >= valid) x.x = 0.f;
                         if (2 * j + 1 >= valid) x.y = 0.f;
                     }
                     odl[j] = x;
-                    odu[j] = __fmul2_rn(x, make_float2(uf[2 * j], uf[2 * j + 1]));
+                    odu[j] = mul2(x, make_float2(uf[2 * j], uf[2 * j + 1]));
                 }
                 // Gate and D·u·gate of the lane's own tokens (the ones it outputs).
                 float2 gt[OP], dug[OP];
@@ -353,7 +392,7 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     for (int m = 0; m < OP; ++m) {
                         const float2 uu = make_float2(uf[2 * m], uf[2 * m + 1]);
                         gt[m] = HAS_Z ? gate2<T>(make_float2(zf[2 * m], zf[2 * m + 1])) : make_float2(1.f, 1.f);
-                        dug[m] = __fmul2_rn(__fmul2_rn(make_float2(skip, skip), uu), gt[m]);
+                        dug[m] = mul2(mul2(make_float2(skip, skip), uu), gt[m]);
                     }
                 }
                 float2 dl[4], du[4];  // (Δ, Δ·u) of tokens (2j, 2j+1), as pairs over tokens
@@ -396,17 +435,22 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
 #pragma unroll
                     for (int q4 = 0; q4 < NR; ++q4) {
                         const float4 bq = br[q4];
-                        const float2 x0 = __fmul2_rn(d2, A2[2 * q4]);
-                        const float2 x1 = __fmul2_rn(d2, A2[2 * q4 + 1]);
+#if SSM_SCAN_SCALAR_X
+                        const float2 x0 = make_float2(dv * A2[2 * q4].x, dv * A2[2 * q4].y);
+                        const float2 x1 = make_float2(dv * A2[2 * q4 + 1].x, dv * A2[2 * q4 + 1].y);
+#else
+                        const float2 x0 = mul2(d2, A2[2 * q4]);
+                        const float2 x1 = mul2(d2, A2[2 * q4 + 1]);
+#endif
                         ao[2 * q4] = make_float2(ex2(x0.x), ex2(x0.y));
                         ao[2 * q4 + 1] = make_float2(ex2(x1.x), ex2(x1.y));
-                        bo[2 * q4] = __fmul2_rn(make_float2(bq.x, bq.y), du2);
-                        bo[2 * q4 + 1] = __fmul2_rn(make_float2(bq.z, bq.w), du2);
+                        bo[2 * q4] = mul2(make_float2(bq.x, bq.y), du2);
+                        bo[2 * q4 + 1] = mul2(make_float2(bq.z, bq.w), du2);
                         if (ZOH) {  // B̄ = Δ·φ(ΔA)·B; x0, x1 hold ΔA·log2e
-                            const float2 n0 = __fmul2_rn(x0, make_float2(kLn2, kLn2));
-                            const float2 n1 = __fmul2_rn(x1, make_float2(kLn2, kLn2));
-                            bo[2 * q4] = __fmul2_rn(bo[2 * q4], make_float2(zoh_phi(n0.x, ao[2 * q4].x), zoh_phi(n0.y, ao[2 * q4].y)));
-                            bo[2 * q4 + 1] = __fmul2_rn(bo[2 * q4 + 1], make_float2(zoh_phi(n1.x, ao[2 * q4 + 1].x),
+                            const float2 n0 = mul2(x0, make_float2(kLn2, kLn2));
+                            const float2 n1 = mul2(x1, make_float2(kLn2, kLn2));
+                            bo[2 * q4] = mul2(bo[2 * q4], make_float2(zoh_phi(n0.x, ao[2 * q4].x), zoh_phi(n0.y, ao[2 * q4].y)));
+                            bo[2 * q4 + 1] = mul2(bo[2 * q4 + 1], make_float2(zoh_phi(n1.x, ao[2 * q4 + 1].x),
                                                                                    zoh_phi(n1.y, ao[2 * q4 + 1].y)));
                         }
                     }
@@ -419,14 +463,14 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     for (int q4 = 0; q4 < NR; ++q4) {
                         const float4 cq = cr[q4];
                         if (q4 == 0) {
-                            acc0 = __fmul2_rn(make_float2(cq.x, cq.y), hs[0]);
-                            acc1 = __fmul2_rn(make_float2(cq.z, cq.w), hs[1]);
+                            acc0 = mul2(make_float2(cq.x, cq.y), hs[0]);
+                            acc1 = mul2(make_float2(cq.z, cq.w), hs[1]);
                         } else {
-                            acc0 = __ffma2_rn(make_float2(cq.x, cq.y), hs[2 * q4], acc0);
-                            acc1 = __ffma2_rn(make_float2(cq.z, cq.w), hs[2 * q4 + 1], acc1);
+                            acc0 = fma2(make_float2(cq.x, cq.y), hs[2 * q4], acc0);
+                            acc1 = fma2(make_float2(cq.z, cq.w), hs[2 * q4 + 1], acc1);
                         }
                     }
-                    const float2 s2 = __fadd2_rn(acc0, acc1);
+                    const float2 s2 = add2(acc0, acc1);
                     p[j] = s2.x + s2.y;
                 };
                 float4 Bnx[NR], Cnx[NR];
@@ -452,7 +496,13 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                         decay_input(j + 1, bcur, an, bn);
                     }
 #pragma unroll
-                    for (int q = 0; q < NQ; ++q) h[q] = __ffma2_rn(ac[q], h[q], bc[q]);
+                    for (int q = 0; q < NQ; ++q) {
+#if SSM_SCAN_SCALAR_H
+                        h[q] = make_float2(fmaf(ac[q].x, h[q].x, bc[q].x), fmaf(ac[q].y, h[q].y, bc[q].y));
+#else
+                        h[q] = fma2(ac[q], h[q], bc[q]);
+#endif
+                    }
                     if (MODE == 0) {
                         if (j > 0) readout(j - 1, hp, Cnx);
                         load_row(Cf, j, Cnx);
@@ -468,7 +518,7 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                         float y[8];
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
-                            const float2 y2 = __ffma2_rn(make_float2(p[2 * m], p[2 * m + 1]), gt[m], dug[m]);
+                            const float2 y2 = fma2(make_float2(p[2 * m], p[2 * m + 1]), gt[m], dug[m]);
                             y[2 * m] = y2.x;
                             y[2 * m + 1] = y2.y;
                         }
@@ -482,8 +532,8 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                             const float keep = g ? p[4 + i] : p[i], send = g ? p[i] : p[4 + i];
                             y[i] = keep + __shfl_xor_sync(FULL, send, 1);
                         }
-                        const float2 y01 = __ffma2_rn(make_float2(y[0], y[1]), gt[0], dug[0]);
-                        const float2 y23 = __ffma2_rn(make_float2(y[2], y[3]), gt[OP - 1], dug[OP - 1]);
+                        const float2 y01 = fma2(make_float2(y[0], y[1]), gt[0], dug[0]);
+                        const float2 y23 = fma2(make_float2(y[2], y[3]), gt[OP - 1], dug[OP - 1]);
                         Pack<T>::store4(out + eo + 4 * g, y01, y23);
                     }
                 }
