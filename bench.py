@@ -432,44 +432,62 @@ def run_ours(args):
             del oi, oy, oh, ows
         out["other_workloads"] = others
 
-    # ---- end to end through the C ABI from pinned host buffers
+    # ---- end to end through the C ABI from pinned host buffers.  Steps
+    # alternate between two buffer sets on two streams, so one step's
+    # device-to-host read overlaps the next step's host-to-device copy (the two
+    # directions use different copy engines); every step still moves its whole
+    # input and output across PCIe inside the timed region.
     if not args.no_e2e:
         names = ("u", "delta", "z", "B", "C")
         small = ("A", "Dskip", "bias")
         host = {k: inp[k].cpu().pin_memory() for k in names + small}
-        dbuf = {k: torch.empty_like(inp[k]) for k in names + small}
-        hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-        hh = torch.empty(hL.shape, dtype=hL.dtype).pin_memory()
-        pe = api.scan_params(dbuf["u"], dbuf["delta"], dbuf["A"], dbuf["B"], dbuf["C"], dbuf["Dskip"],
-                             dbuf["z"], dbuf["bias"], None, y=y, hL=hL, workspace=ws)
+        streams = [stream, torch.cuda.Stream(dev)]
+        sets = []
+        for si_ in range(2):
+            dbuf = {k: torch.empty_like(inp[k]) for k in names + small}
+            ye, he = torch.empty_like(y), torch.empty_like(hL)
+            wse = torch.empty_like(ws)
+            hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+            hh = torch.empty(hL.shape, dtype=hL.dtype).pin_memory()
+            pe = api.scan_params(dbuf["u"], dbuf["delta"], dbuf["A"], dbuf["B"], dbuf["C"], dbuf["Dskip"],
+                                 dbuf["z"], dbuf["bias"], None, y=ye, hL=he, workspace=wse)
+            sets.append((dbuf, ye, he, hy, hh, pe))
         h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = hy.numel() * hy.element_size() + hh.numel() * hh.element_size()
+        d2h = y.numel() * y.element_size() + hL.numel() * hL.element_size()
 
-        def e2e_step():
-            for k, t in host.items():
-                dbuf[k].copy_(t, non_blocking=True)
-            capi.ssm_scan_fwd(pe, sh)
-            hy.copy_(y, non_blocking=True)
-            hh.copy_(hL, non_blocking=True)
+        def e2e_step(i):
+            dbuf, ye, he, hy, hh, pe = sets[i % 2]
+            st_ = streams[i % 2]
+            with torch.cuda.stream(st_):
+                for k, t in host.items():
+                    dbuf[k].copy_(t, non_blocking=True)
+                capi.ssm_scan_fwd(pe, st_.cuda_stream)
+                hy.copy_(ye, non_blocking=True)
+                hh.copy_(he, non_blocking=True)
 
-        for _ in range(max(3, args.warmup)):
-            e2e_step()
+        for i in range(max(3, args.warmup)):
+            e2e_step(i)
         torch.cuda.synchronize(dev)
-        ksteps = max(3, min(args.steps, 50))
+        ksteps = max(4, min(args.steps, 50))
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(ksteps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(streams[0])
+        streams[1].wait_event(e0)
+        for i in range(ksteps):
+            e2e_step(i)
+        done1 = torch.cuda.Event()
+        done1.record(streams[1])
+        streams[0].wait_event(done1)
+        e1.record(streams[0])
         torch.cuda.synchronize(dev)
         barrier()
         ms = allmax(e0.elapsed_time(e1))
         out["e2e"] = {"value": elems * ksteps * world / (ms / 1e3) / 1e9, "unit": UNIT,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ksteps,
-                      "ms_per_step": ms / ksteps}
+                      "ms_per_step": ms / ksteps,
+                      "pipelining": "two buffer sets on two streams (copy directions overlap)"}
         out["gpu_launches"] += launches_per_step * ksteps
-        del host, dbuf
+        del host, sets
 
     # ---- decode: 64 consecutive tokens, L2 flushed before each (cold state as in a deep stack)
     if not args.no_decode:

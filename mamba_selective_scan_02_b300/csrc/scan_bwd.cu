@@ -26,7 +26,7 @@
 // dC = Σ ŷ·h is formed per tile from the stored states; the tile's [16 × N]
 // sums are added to memory.  dA, dD and dbias sum over tokens in registers
 // and are added once per item.  Each tile's global loads are issued one tile
-// ahead, into registers.
+// ahead into registers (three tiles ahead in the checkpoint pass).
 #include <algorithm>
 
 #include "ssm_device.cuh"
@@ -197,8 +197,12 @@ bwd_ckpt_kernel(const BwdArgs a) {
                 f.d[h8].template load<VEC>(drow, t0 + OWN * g + 8 * h8, L);
             }
         };
-        Pre cur;
+        // three tiles in flight: a tile's 16 tokens take far less time than a
+        // load from memory
+        Pre cur, nx1, nx2;
         fetch(tb, cur);
+        if (tb + TS < te) fetch(tb + TS, nx1);
+        if (tb + 2 * TS < te) fetch(tb + 2 * TS, nx2);
         for (int t0 = tb; t0 < te; t0 += TS) {
             // the state entering this tile is its checkpoint
             float4 *ck = reinterpret_cast<float4 *>(a.ckpt) + ((size_t)it.grp * a.ntiles + t0 / TS) * 64;
@@ -222,7 +226,9 @@ bwd_ckpt_kernel(const BwdArgs a) {
                 }
             }
             __syncwarp();
-            if (t0 + TS < te) fetch(t0 + TS, cur);
+            cur = nx1;
+            nx1 = nx2;
+            if (t0 + 3 * TS < te) fetch(t0 + 3 * TS, nx2);
 #pragma unroll 4
             for (int t = 0; t < TS; ++t) {
                 const float dl = Dl[c * TSP + t], du = Du[c * TSP + t];
