@@ -333,6 +333,18 @@ const char *ssm_status_string(ssm_status s);
  * the MUFU ex2 throughput the scan's roofline is taken against. */
 ssm_status ssm_bench_mufu_ex2(float *sink, int blocks, int iters, ssm_stream_t stream);
 
+/* Self-test of the device-side failure path (not part of the method).
+ * Clears the status word and a flag in the workspace's 256-byte header, then
+ * launches one thread that waits for that flag — which nothing sets — with the
+ * bounded wait the chained scans use for a predecessor's hand-off.  After
+ * `polls` polls (1 .. 2^24; about a microsecond each) it records
+ * SSM_ERR_TIMEOUT in the status word, exactly as a scan whose hand-off never
+ * came would.  ssm_workspace_status then returns SSM_ERR_TIMEOUT and the
+ * context stays usable.  workspace: a device buffer of at least 256 bytes,
+ * 16-byte aligned.  Returns SSM_ERR_INVALID_ARG for bad arguments (nothing
+ * launched) or SSM_ERR_CUDA if the launch fails. */
+ssm_status ssm_selftest_flag_wait(void *workspace, size_t workspace_bytes, int polls, ssm_stream_t stream);
+
 /* Library build identification, e.g. "libssmscan sm_103a". */
 const char *ssm_version(void);
 

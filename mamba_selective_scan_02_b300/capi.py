@@ -137,6 +137,8 @@ def lib():
             L.ssm_status_string.argtypes = [ctypes.c_int]
             L.ssm_bench_mufu_ex2.restype = ctypes.c_int
             L.ssm_bench_mufu_ex2.argtypes = [_vp, ctypes.c_int, ctypes.c_int, _vp]
+            L.ssm_selftest_flag_wait.restype = ctypes.c_int
+            L.ssm_selftest_flag_wait.argtypes = [_vp, ctypes.c_size_t, ctypes.c_int, _vp]
             L.ssm_version.restype = ctypes.c_char_p
             L.ssm_version.argtypes = []
             _lib = L
@@ -207,3 +209,7 @@ def ssm_workspace_status(workspace: int, stream: int) -> int:
 
 def ssm_bench_mufu_ex2(sink: int, blocks: int, iters: int, stream: int) -> int:
     return lib().ssm_bench_mufu_ex2(sink, blocks, iters, stream)
+
+
+def ssm_selftest_flag_wait(workspace: int, nbytes: int, polls: int, stream: int) -> int:
+    return lib().ssm_selftest_flag_wait(workspace, nbytes, polls, stream)

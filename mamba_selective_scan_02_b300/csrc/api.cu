@@ -453,6 +453,16 @@ ssm_status ssm_bench_mufu_ex2(float *sink, int blocks, int iters, ssm_stream_t s
                : SSM_ERR_CUDA;
 }
 
+ssm_status ssm_selftest_flag_wait(void *workspace, size_t workspace_bytes, int polls, ssm_stream_t stream) {
+    if (!workspace || workspace_bytes < kHeader || !aligned16(workspace) || polls < 1 || polls > (1 << 24))
+        return SSM_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(workspace, 0, kHeader, st) != cudaSuccess) return SSM_ERR_CUDA;
+    int *hdr = static_cast<int *>(workspace);
+    // the status word at offset 0; the never-set flag past the work counters
+    return ssm::flag_wait_selftest_launch(hdr, hdr + 16, polls, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 const char *ssm_version(void) { return "libssmscan sm_103a"; }
 
 }  // extern "C"

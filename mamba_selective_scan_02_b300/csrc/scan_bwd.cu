@@ -41,14 +41,6 @@ constexpr int SPT = 8;                  // states per lane
 constexpr int kBwdFlagLimit = 1 << 24;  // polls of a neighbour's flag before giving up
 constexpr int kBwdWarpsPerSM = 8;
 
-__device__ __forceinline__ int ld_acquire_b(const int *p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_b(int *p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 __device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.0f + ex2(-x * kLog2e)); }
 
@@ -161,13 +153,10 @@ bwd_ckpt_kernel(const BwdArgs a) {
         if (it.k == 0) {
             src = a.h0 ? a.h0 + ((size_t)it.b * D + d) * N : nullptr;
         } else {
-            if (lane == 0) {
-                int polls = 0;
-                while (ld_acquire_b(a.flags_fwd + it.grp) < it.k && ++polls < kBwdFlagLimit) __nanosleep(64);
-                if (polls >= kBwdFlagLimit) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
-            }
+            if (lane == 0 && !wait_flag(a.flags_fwd + it.grp, it.k, kBwdFlagLimit))
+                record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
             __syncwarp();
-            (void)ld_acquire_b(a.flags_fwd + it.grp);
+            (void)flag_acquire(a.flags_fwd + it.grp);
             src = a.carry_fwd + ((size_t)it.b * D + d) * N;
             cg = true;
         }
@@ -261,7 +250,7 @@ bwd_ckpt_kernel(const BwdArgs a) {
                 }
             }
             __syncwarp();
-            if (lane == 0) st_release_b(a.flags_fwd + it.grp, it.k + 1);
+            if (lane == 0) flag_release(a.flags_fwd + it.grp, it.k + 1);
         }
     }
 }
@@ -329,13 +318,10 @@ bwd_rev_kernel(const BwdArgs a) {
         if (r == 0) {
             src = a.dhL ? a.dhL + ((size_t)it.b * D + d) * N : nullptr;
         } else {
-            if (lane == 0) {
-                int polls = 0;
-                while (ld_acquire_b(a.flags_rev + it.grp) < r && ++polls < kBwdFlagLimit) __nanosleep(64);
-                if (polls >= kBwdFlagLimit) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
-            }
+            if (lane == 0 && !wait_flag(a.flags_rev + it.grp, r, kBwdFlagLimit))
+                record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
             __syncwarp();
-            (void)ld_acquire_b(a.flags_rev + it.grp);
+            (void)flag_acquire(a.flags_rev + it.grp);
             src = a.carry_rev + ((size_t)it.b * D + d) * N;
             cg = true;
         }
@@ -621,7 +607,7 @@ bwd_rev_kernel(const BwdArgs a) {
                 }
             }
             __syncwarp();
-            if (lane == 0) st_release_b(a.flags_rev + it.grp, r + 1);
+            if (lane == 0) flag_release(a.flags_rev + it.grp, r + 1);
         } else if (a.dh0 && live) {
             float *dst = a.dh0 + ((size_t)it.b * D + d) * N;
 #pragma unroll

@@ -151,14 +151,6 @@ template <> struct Pack<__nv_bfloat16> {
     }
 };
 
-__device__ __forceinline__ int ld_acquire(const int *p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release(int *p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 // One work item: a group of CPW channels of one sequence, one chunk of tokens.
 struct Item {
@@ -292,13 +284,10 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             if (it.k == 0) {
                 src = a.h0 ? a.h0 + ((size_t)it.b * D + d) * N : nullptr;
             } else if (chained) {
-                if (lane == 0) {
-                    int polls = 0;
-                    while (ld_acquire(a.flags + it.grp) < it.k && ++polls < kFlagLimit) __nanosleep(64);
-                    if (polls >= kFlagLimit) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
-                }
+                if (lane == 0 && !wait_flag(a.flags + it.grp, it.k, kFlagLimit))
+                    record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
                 __syncwarp();
-                (void)ld_acquire(a.flags + it.grp);  // every lane orders its reads after the hand-off
+                (void)flag_acquire(a.flags + it.grp);  // every lane orders its reads after the hand-off
                 src = a.carry + ((size_t)it.b * D + d) * N;
                 cg = true;
             } else {
@@ -584,7 +573,7 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 // The warp barrier orders every lane's state stores before lane
                 // 0's release store; a reader that acquires the flag sees them.
                 __syncwarp();
-                if (lane == 0) st_release(a.flags + it.grp, it.k + 1);
+                if (lane == 0) flag_release(a.flags + it.grp, it.k + 1);
             }
         } else if (live) {
 #pragma unroll

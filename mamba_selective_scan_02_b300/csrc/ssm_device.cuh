@@ -233,4 +233,27 @@ __device__ __forceinline__ void record_error(int *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// ---------------------------------------------------------------- chained hand-offs
+// A work item publishes "chunks done" with a release store after writing its
+// state; the item that continues from it waits with acquire loads.
+__device__ __forceinline__ int flag_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void flag_release(int *p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Polls *flag until it reaches `target`, sleeping between polls, at most
+// `limit` polls.  Returns false if it gave up; callers record SSM_ERR_TIMEOUT
+// and carry on, so a launch always ends.
+__device__ __forceinline__ bool wait_flag(const int *flag, int target, int limit) {
+    int polls = 0;
+    while (flag_acquire(flag) < target) {
+        if (++polls >= limit) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
 }  // namespace ssm

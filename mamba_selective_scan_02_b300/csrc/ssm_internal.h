@@ -121,5 +121,6 @@ constexpr int kBwdTile = 16;             // tokens per checkpoint / recompute ti
 constexpr int kBwdChunk = 256;           // tokens per work item of the backward passes
 cudaError_t conv_step_launch(const ConvStepArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t mufu_ex2_launch(float *sink, int blocks, int iters, cudaStream_t stream);
+cudaError_t flag_wait_selftest_launch(int *status, const int *flag, int polls, cudaStream_t stream);
 
 }  // namespace ssm

@@ -310,3 +310,12 @@ def valid_ssd(**over):
 def test_ssd_rejects_before_launch(over, code):
     assert capi.ssm_ssd_fwd(valid_ssd(**over), None) == code
     assert capi.lib().ssm_ssd_fwd(None, None) == capi.SSM_ERR_INVALID_ARG
+
+
+def test_selftest_flag_wait_rejects_before_launch():
+    lib = capi.lib()
+    assert lib.ssm_selftest_flag_wait(None, 256, 10, None) == capi.SSM_ERR_INVALID_ARG
+    assert lib.ssm_selftest_flag_wait(ctypes.c_void_p(FAKE), 100, 10, None) == capi.SSM_ERR_INVALID_ARG
+    assert lib.ssm_selftest_flag_wait(ctypes.c_void_p(FAKE + 8), 256, 10, None) == capi.SSM_ERR_INVALID_ARG
+    assert lib.ssm_selftest_flag_wait(ctypes.c_void_p(FAKE), 256, 0, None) == capi.SSM_ERR_INVALID_ARG
+    assert lib.ssm_selftest_flag_wait(ctypes.c_void_p(FAKE), 256, (1 << 24) + 1, None) == capi.SSM_ERR_INVALID_ARG
