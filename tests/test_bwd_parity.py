@@ -76,7 +76,9 @@ def run_both(inp, zoh, chunk_len=0, threads=8):
 @pytest.mark.parametrize("gate", [True, False])
 @pytest.mark.parametrize("shape,chunk", [((2, 40, 300), 64),     # ragged D and L: scalar loads, partial tile
                                          ((2, 48, 256), 64),     # aligned: vector loads, four chained chunks
-                                         ((1, 17, 33), 0)])      # one chunk, three partial tiles
+                                         ((1, 17, 33), 0),       # one chunk, three partial tiles
+                                         ((2, 16, 16), 0),       # exactly one tile
+                                         ((1, 20, 1), 0)])       # a single token
 def test_bwd_every_element(io, N, zoh, gate, shape, chunk):
     b, D, L = shape
     inp = draw(io, b, D, N, L, seed=L + N + 7 * zoh, gate=gate)
