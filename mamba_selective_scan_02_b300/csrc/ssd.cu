@@ -127,33 +127,47 @@ ssd_kernel(const SsdArgs a) {
     const float Dh = a.Dskip ? a.Dskip[h] : 0.f;
     const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
 
-    // the state rows 16w .. 16w+15 of this warp, all NS columns, fp32:
-    // Sacc[nt][0..3] holds (p = 16w+gid, n = 8nt+2tig, +1) and (p + 8, same n)
-    float Sacc[NS / 8][4];
+    // the state S[p][n] in fp32: warp w owns columns n = 32w .. 32w+31 for all
+    // P rows; Sacc[mt][nt][0..3] holds (p = 16mt+gid, n = 32w+8nt+2tig, +1)
+    // and (p + 8, same n)
+    float Sacc[P / 16][4][4];
 #pragma unroll
-    for (int nt = 0; nt < NS / 8; ++nt) {
+    for (int mt = 0; mt < P / 16; ++mt) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int p = 16 * w + gid + 8 * (e >> 1), n = 8 * nt + 2 * tig + (e & 1);
-            Sacc[nt][e] = a.h0 ? a.h0[(((size_t)b * H + h) * P + p) * NS + n] : 0.f;
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int p = 16 * mt + gid + 8 * (e >> 1), n = 32 * w + 8 * nt + 2 * tig + (e & 1);
+                Sacc[mt][nt][e] = a.h0 ? a.h0[(((size_t)b * H + h) * P + p) * NS + n] : 0.f;
+            }
         }
     }
 
-    // the first chunk's inherited state, as its bf16 operand pair
+    // the inherited state as its bf16 operand pair, [p][n] in S (value) and Sl
     auto store_state = [&]() {
 #pragma unroll
-        for (int nt = 0; nt < NS / 8; ++nt) {
-            const int n = 8 * nt + 2 * tig;
-            uint32_t hi, lo;
-            split_bf16(Sacc[nt][0], Sacc[nt][1], hi, lo);
-            *reinterpret_cast<uint32_t *>(sm.S + swz(16 * w + gid, n, BS)) = hi;
-            *reinterpret_cast<uint32_t *>(sm.Sl + swz(16 * w + gid, n, BS)) = lo;
-            split_bf16(Sacc[nt][2], Sacc[nt][3], hi, lo);
-            *reinterpret_cast<uint32_t *>(sm.S + swz(16 * w + gid + 8, n, BS)) = hi;
-            *reinterpret_cast<uint32_t *>(sm.Sl + swz(16 * w + gid + 8, n, BS)) = lo;
+        for (int mt = 0; mt < P / 16; ++mt) {
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int p = 16 * mt + gid, n = 32 * w + 8 * nt + 2 * tig;
+                uint32_t hi, lo;
+                split_bf16(Sacc[mt][nt][0], Sacc[mt][nt][1], hi, lo);
+                *reinterpret_cast<uint32_t *>(sm.S + swz(p, n, BS)) = hi;
+                *reinterpret_cast<uint32_t *>(sm.Sl + swz(p, n, BS)) = lo;
+                split_bf16(Sacc[mt][nt][2], Sacc[mt][nt][3], hi, lo);
+                *reinterpret_cast<uint32_t *>(sm.S + swz(p + 8, n, BS)) = hi;
+                *reinterpret_cast<uint32_t *>(sm.Sl + swz(p + 8, n, BS)) = lo;
+            }
         }
     };
     store_state();
+    __syncthreads();
+
+    // the decay-masked block Λ ∘ C·Bᵀ lives, as a bf16 value / remainder pair
+    // [i][j], in the state buffers while they are free (after the read-out of
+    // the inherited state, before the new state is stored)
+    __nv_bfloat16 *Mh = sm.S, *Ml = sm.Sl;
+    constexpr int MS = Q;                           // row of the masked block
 
     const int nchunks = (L + Q - 1) / Q;
     for (int ck = 0; ck < nchunks; ++ck) {
@@ -200,105 +214,125 @@ ssd_kernel(const SsdArgs a) {
         __syncthreads();
         if (tid < Q) sm.wsc[tid] = ex2((sm.cum[Q - 1] - sm.cum[tid]) * kLog2e) * sm.delta[tid];
 
-        const int r0 = 16 * w;                    // this warp's rows (tokens) of the chunk
-        const float cr0 = sm.cum[r0 + gid], cr1 = sm.cum[r0 + gid + 8];
-
-        // ---- Y = diag(e^cum) · C · S_inᵀ   (rows r0.., all P columns)
-        float Y[P / 8][4];
+        // ---- Y = diag(e^cum) · C · S_inᵀ: all 64 rows, columns p = 16w .. 16w+15
+        float Y[Q / 16][2][4];
 #pragma unroll
-        for (int nt = 0; nt < P / 8; ++nt) Y[nt][0] = Y[nt][1] = Y[nt][2] = Y[nt][3] = 0.f;
+        for (int mt = 0; mt < Q / 16; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) Y[mt][nt][0] = Y[mt][nt][1] = Y[mt][nt][2] = Y[mt][nt][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < NS / 16; ++ks) {
-            uint32_t af[4];
-            frag_a(af, sm.C, BS, r0, 16 * ks, lane);
+            uint32_t bf[4], bl[4];
+            frag_b_nk(bf, sm.S, BS, 16 * w, 16 * ks, lane);
+            frag_b_nk(bl, sm.Sl, BS, 16 * w, 16 * ks, lane);
 #pragma unroll
-            for (int np = 0; np < P / 16; ++np) {
-                uint32_t bf[4], bl[4];
-                frag_b_nk(bf, sm.S, BS, 16 * np, 16 * ks, lane);
-                frag_b_nk(bl, sm.Sl, BS, 16 * np, 16 * ks, lane);
-                mma16816(Y[2 * np], af, bf[0], bf[1]);
-                mma16816(Y[2 * np + 1], af, bf[2], bf[3]);
-                mma16816(Y[2 * np], af, bl[0], bl[1]);
-                mma16816(Y[2 * np + 1], af, bl[2], bl[3]);
+            for (int mt = 0; mt < Q / 16; ++mt) {
+                uint32_t af[4];
+                frag_a(af, sm.C, BS, 16 * mt, 16 * ks, lane);
+                mma16816(Y[mt][0], af, bf[0], bf[1]);
+                mma16816(Y[mt][1], af, bf[2], bf[3]);
+                mma16816(Y[mt][0], af, bl[0], bl[1]);
+                mma16816(Y[mt][1], af, bl[2], bl[3]);
             }
         }
+#pragma unroll
+        for (int mt = 0; mt < Q / 16; ++mt) {
+            const float e0 = ex2(sm.cum[16 * mt + gid] * kLog2e), e1 = ex2(sm.cum[16 * mt + gid + 8] * kLog2e);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                Y[mt][nt][0] *= e0;
+                Y[mt][nt][1] *= e0;
+                Y[mt][nt][2] *= e1;
+                Y[mt][nt][3] *= e1;
+            }
+        }
+
+        // ---- G = C · Bᵀ for rows 16w .. 16w+15 on the causal part (columns
+        // j <= 16w + 15), masked by Λ into the shared value / remainder pair
         {
-            const float e0 = ex2(cr0 * kLog2e), e1 = ex2(cr1 * kLog2e);
+            const int r0 = 16 * w;
+            const int njt = 2 * (w + 1);
+            float G[Q / 8][4];
 #pragma unroll
-            for (int nt = 0; nt < P / 8; ++nt) {
-                Y[nt][0] *= e0;
-                Y[nt][1] *= e0;
-                Y[nt][2] *= e1;
-                Y[nt][3] *= e1;
+            for (int nt = 0; nt < Q / 8; ++nt) G[nt][0] = G[nt][1] = G[nt][2] = G[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < NS / 16; ++ks) {
+                uint32_t af[4];
+                frag_a(af, sm.C, BS, r0, 16 * ks, lane);
+#pragma unroll
+                for (int np = 0; np < Q / 16; ++np) {
+                    if (2 * np < njt) {
+                        uint32_t bf[4];
+                        frag_b_nk(bf, sm.B, BS, 16 * np, 16 * ks, lane);
+                        mma16816(G[2 * np], af, bf[0], bf[1]);
+                        mma16816(G[2 * np + 1], af, bf[2], bf[3]);
+                    }
+                }
+            }
+            __syncthreads();                         // every warp is done reading S, Sl
+            const float cr0 = sm.cum[r0 + gid], cr1 = sm.cum[r0 + gid + 8];
+#pragma unroll
+            for (int nt = 0; nt < Q / 8; ++nt) {
+                if (nt < njt) {
+                    const int j0 = 8 * nt + 2 * tig;
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = r0 + gid + 8 * (e >> 1), j = j0 + (e & 1);
+                        const float ci = (e >> 1) ? cr1 : cr0;
+                        v[e] = j <= i ? G[nt][e] * ex2((ci - sm.cum[j]) * kLog2e) * sm.delta[j] : 0.f;
+                    }
+                    uint32_t hi, lo;
+                    split_bf16(v[0], v[1], hi, lo);
+                    *reinterpret_cast<uint32_t *>(Mh + swz(r0 + gid, j0, MS)) = hi;
+                    *reinterpret_cast<uint32_t *>(Ml + swz(r0 + gid, j0, MS)) = lo;
+                    split_bf16(v[2], v[3], hi, lo);
+                    *reinterpret_cast<uint32_t *>(Mh + swz(r0 + gid + 8, j0, MS)) = hi;
+                    *reinterpret_cast<uint32_t *>(Ml + swz(r0 + gid + 8, j0, MS)) = lo;
+                }
             }
         }
+        __syncthreads();
 
-        // ---- G = C · Bᵀ on the causal part (columns j <= r0 + 15), then
-        // Λ-masked into bf16 A fragments, and Y += (G ∘ Λ) · X
-        const int njt = 2 * (w + 1);               // 8-column tiles at or left of the diagonal block
-        float G[Q / 8][4];
+        // ---- Y += (Λ ∘ C·Bᵀ) · X on the causal blocks (row block mt, column block ks <= mt)
 #pragma unroll
-        for (int nt = 0; nt < Q / 8; ++nt) G[nt][0] = G[nt][1] = G[nt][2] = G[nt][3] = 0.f;
+        for (int ks = 0; ks < Q / 16; ++ks) {
+            uint32_t bf[4];
+            frag_b_kn(bf, sm.x, XS, 16 * w, 16 * ks, lane);
 #pragma unroll
-        for (int ks = 0; ks < NS / 16; ++ks) {
-            uint32_t af[4];
-            frag_a(af, sm.C, BS, r0, 16 * ks, lane);
-#pragma unroll
-            for (int np = 0; np < Q / 16; ++np) {
-                if (2 * np < njt) {
-                    uint32_t bf[4];
-                    frag_b_nk(bf, sm.B, BS, 16 * np, 16 * ks, lane);
-                    mma16816(G[2 * np], af, bf[0], bf[1]);
-                    mma16816(G[2 * np + 1], af, bf[2], bf[3]);
+            for (int mt = 0; mt < Q / 16; ++mt) {
+                if (ks <= mt) {
+                    uint32_t mh[4], ml[4];
+                    frag_a(mh, Mh, MS, 16 * mt, 16 * ks, lane);
+                    frag_a(ml, Ml, MS, 16 * mt, 16 * ks, lane);
+                    mma16816(Y[mt][0], mh, bf[0], bf[1]);
+                    mma16816(Y[mt][1], mh, bf[2], bf[3]);
+                    mma16816(Y[mt][0], ml, bf[0], bf[1]);
+                    mma16816(Y[mt][1], ml, bf[2], bf[3]);
                 }
-            }
-        }
-#pragma unroll
-        for (int kk = 0; kk < Q / 16; ++kk) {
-            if (kk > w) break;
-            uint32_t mf[4], ml[4];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int nt = 2 * kk + half;
-                const int j0 = 8 * nt + 2 * tig;
-                float v[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = r0 + gid + 8 * (e >> 1), j = j0 + (e & 1);
-                    const float ci = (e >> 1) ? cr1 : cr0;
-                    v[e] = j <= i ? G[nt][e] * ex2((ci - sm.cum[j]) * kLog2e) * sm.delta[j] : 0.f;
-                }
-                split_bf16(v[0], v[1], mf[2 * half], ml[2 * half]);
-                split_bf16(v[2], v[3], mf[2 * half + 1], ml[2 * half + 1]);
-            }
-#pragma unroll
-            for (int np = 0; np < P / 16; ++np) {
-                uint32_t bf[4];
-                frag_b_kn(bf, sm.x, XS, 16 * np, 16 * kk, lane);
-                mma16816(Y[2 * np], mf, bf[0], bf[1]);
-                mma16816(Y[2 * np + 1], mf, bf[2], bf[3]);
-                mma16816(Y[2 * np], ml, bf[0], bf[1]);
-                mma16816(Y[2 * np + 1], ml, bf[2], bf[3]);
             }
         }
 
         // ---- y = Y + D·x, to memory
 #pragma unroll
-        for (int nt = 0; nt < P / 8; ++nt) {
+        for (int mt = 0; mt < Q / 16; ++mt) {
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int i = r0 + gid + 8 * hr, t = t0 + i, p = 8 * nt + 2 * tig;
-                if (t < L) {
-                    const __nv_bfloat162 xv = *reinterpret_cast<const __nv_bfloat162 *>(sm.x + swz(i, p, XS));
-                    const float y0 = fmaf(Dh, __low2float(xv), Y[nt][2 * hr]);
-                    const float y1 = fmaf(Dh, __high2float(xv), Y[nt][2 * hr + 1]);
-                    *reinterpret_cast<uint32_t *>(yg + (((size_t)b * L + t) * H + h) * P + p) = pack_bf16(y0, y1);
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int i = 16 * mt + gid + 8 * hr, t = t0 + i, p = 16 * w + 8 * nt + 2 * tig;
+                    if (t < L) {
+                        const __nv_bfloat162 xv = *reinterpret_cast<const __nv_bfloat162 *>(sm.x + swz(i, p, XS));
+                        const float y0 = fmaf(Dh, __low2float(xv), Y[mt][nt][2 * hr]);
+                        const float y1 = fmaf(Dh, __high2float(xv), Y[mt][nt][2 * hr + 1]);
+                        *reinterpret_cast<uint32_t *>(yg + (((size_t)b * L + t) * H + h) * P + p) = pack_bf16(y0, y1);
+                    }
                 }
             }
         }
 
         // ---- S_out = e^{cum_{Q−1}} S_in + Xᵀ · diag(w) · B,  w_j = e^{cum_{Q−1} − cum_j}·Δ_j
-        __syncthreads();                            // every warp is done reading B and S
+        __syncthreads();                            // every warp is done reading B, C and the masked block
         const float clast = sm.cum[Q - 1];
         for (int i = tid; i < Q * (NS / 2); i += kThreads) {
             const int r = i / (NS / 2), q = i % (NS / 2);
@@ -314,40 +348,49 @@ ssd_kernel(const SsdArgs a) {
         {
             const float et = ex2(clast * kLog2e);
 #pragma unroll
-            for (int nt = 0; nt < NS / 8; ++nt) {
-                Sacc[nt][0] *= et;
-                Sacc[nt][1] *= et;
-                Sacc[nt][2] *= et;
-                Sacc[nt][3] *= et;
-            }
+            for (int mt = 0; mt < P / 16; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) Sacc[mt][nt][e] *= et;
 #pragma unroll
             for (int ks = 0; ks < Q / 16; ++ks) {
-                uint32_t af[4];
-                frag_a_t(af, sm.x, XS, r0, 16 * ks, lane);   // A[p][j] = x[j][p]
+                uint32_t bh0[4], bl0[4], bh1[4], bl1[4];
+                frag_b_kn(bh0, sm.B, BS, 32 * w, 16 * ks, lane);
+                frag_b_kn(bl0, sm.C, BS, 32 * w, 16 * ks, lane);
+                frag_b_kn(bh1, sm.B, BS, 32 * w + 16, 16 * ks, lane);
+                frag_b_kn(bl1, sm.C, BS, 32 * w + 16, 16 * ks, lane);
 #pragma unroll
-                for (int np = 0; np < NS / 16; ++np) {
-                    uint32_t bf[4], bl[4];
-                    frag_b_kn(bf, sm.B, BS, 16 * np, 16 * ks, lane);
-                    frag_b_kn(bl, sm.C, BS, 16 * np, 16 * ks, lane);
-                    mma16816(Sacc[2 * np], af, bf[0], bf[1]);
-                    mma16816(Sacc[2 * np + 1], af, bf[2], bf[3]);
-                    mma16816(Sacc[2 * np], af, bl[0], bl[1]);
-                    mma16816(Sacc[2 * np + 1], af, bl[2], bl[3]);
+                for (int mt = 0; mt < P / 16; ++mt) {
+                    uint32_t af[4];
+                    frag_a_t(af, sm.x, XS, 16 * mt, 16 * ks, lane);   // A[p][j] = x[j][p]
+                    mma16816(Sacc[mt][0], af, bh0[0], bh0[1]);
+                    mma16816(Sacc[mt][1], af, bh0[2], bh0[3]);
+                    mma16816(Sacc[mt][2], af, bh1[0], bh1[1]);
+                    mma16816(Sacc[mt][3], af, bh1[2], bh1[3]);
+                    mma16816(Sacc[mt][0], af, bl0[0], bl0[1]);
+                    mma16816(Sacc[mt][1], af, bl0[2], bl0[3]);
+                    mma16816(Sacc[mt][2], af, bl1[0], bl1[1]);
+                    mma16816(Sacc[mt][3], af, bl1[2], bl1[3]);
                 }
             }
         }
-        // the next chunk's inherited state, as its bf16 operand pair
+        // the next chunk's inherited state, as its bf16 operand pair (the
+        // masked block in the same buffers is no longer read)
         store_state();
         __syncthreads();
     }
 
     if (a.hL) {
 #pragma unroll
-        for (int nt = 0; nt < NS / 8; ++nt) {
+        for (int mt = 0; mt < P / 16; ++mt) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int p = 16 * w + gid + 8 * (e >> 1), n = 8 * nt + 2 * tig + (e & 1);
-                a.hL[(((size_t)b * H + h) * P + p) * NS + n] = Sacc[nt][e];
+            for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int p = 16 * mt + gid + 8 * (e >> 1), n = 32 * w + 8 * nt + 2 * tig + (e & 1);
+                    a.hL[(((size_t)b * H + h) * P + p) * NS + n] = Sacc[mt][nt][e];
+                }
             }
         }
     }
