@@ -21,10 +21,9 @@
 //   2. reverse pass: chunks in reverse order, chunk k starting from the adjoint
 //      chunk k+1 hands over.  Per tile it recomputes the 16 states from the
 //      checkpoint into shared memory, then walks the tile backwards.
-// dB and dC sum over channels: per token a warp folds dB over its channels
-// with a transposed butterfly (each shuffle halves the values a lane holds);
-// dC = Σ ŷ·h is formed per tile from the stored states; the tile's [16 × N]
-// sums are added to memory.  dA, dD and dbias sum over tokens in registers
+// dB and dC sum over channels, per tile: dC = Σ ŷ·h from the stored states
+// before the walk back, dB from the per-token partials each lane leaves in the
+// spent state slots during it; the tile's [16 × N] sums are added to memory.  dA, dD and dbias sum over tokens in registers
 // and are added once per item.  Each tile's global loads are issued one tile
 // ahead into registers (three tiles ahead in the checkpoint pass).
 #include <algorithm>
@@ -443,10 +442,11 @@ bwd_rev_kernel(const BwdArgs a) {
             }
             __syncwarp();
 
-            // ---- dC of the tile: Σ over the warp's channels of ŷ·h, read back
-            // from the stored states (lane: one token, half of the states; the
-            // channel order is staggered by token against bank conflicts)
-            {
+            // ---- channel sums over the tile, read back from the per-token
+            // [t][half][lane] buffer Hs (lane: one token, half of the states; the
+            // channel order is staggered by token against bank conflicts):
+            // Σ_c weight[c][t]·Hs[t][c] into row m (0: dB, 1: dC) of the sums
+            auto channel_sum = [&](int m, bool weighted) {
                 constexpr int HN = NP / 2;            // states per lane here
                 const int t = lane >> 1, hh = lane & 1;
                 float acc[HN];
@@ -455,7 +455,7 @@ bwd_rev_kernel(const BwdArgs a) {
 #pragma unroll 4
                 for (int i = 0; i < CPW; ++i) {
                     const int cc = (i + t) % CPW;
-                    const float y = sm.Yh[cc * TSP + t];
+                    const float y = weighted ? sm.Yh[cc * TSP + t] : 1.f;
                     if (NG == 2) {
                         const float4 p0 = sm.Hs[(t * 2) * 32 + 2 * cc + hh], p1 = sm.Hs[(t * 2 + 1) * 32 + 2 * cc + hh];
                         acc[0] = fmaf(y, p0.x, acc[0]); acc[1] = fmaf(y, p0.y, acc[1]);
@@ -469,8 +469,10 @@ bwd_rev_kernel(const BwdArgs a) {
                     }
                 }
 #pragma unroll
-                for (int j = 0; j < HN; ++j) sm.acc[(t * 2 + 1) * NP + HN * hh + j] = acc[j];
-            }
+                for (int j = 0; j < HN; ++j) sm.acc[(t * 2 + m) * NP + HN * hh + j] = acc[j];
+            };
+            // dC = Σ_c ŷ·h from the recomputed states
+            channel_sum(1, true);
 
             // ---- the adjoint, backwards through the tile
             float2 hcur[NQ];
@@ -547,27 +549,16 @@ bwd_rev_kernel(const BwdArgs a) {
                     sm.Odd[e] = ddr;
                     if (HAS_Z) sm.Odz[e] = sm.Gp[e] * sm.Sp[e];
                 }
-                // dB: sum the lane's 8 partials over the warp's channels; each
-                // shuffle step halves what a lane holds, the rest add in full
-                constexpr int B0 = NG == 2 ? 1 : 0;     // first lane bit that selects a channel
-#pragma unroll
-                for (int s = 0; s < 3; ++s) {
-                    const int w = 4 >> s;
-                    const bool hb = (lane >> (B0 + s)) & 1;
-#pragma unroll
-                    for (int j = 0; j < w; ++j) {
-                        const float lo = v[j], hi = v[j + w];
-                        const float send = hb ? lo : hi, keep = hb ? hi : lo;
-                        v[j] = keep + __shfl_xor_sync(FULL, send, 1 << (B0 + s));
-                    }
-                }
-#pragma unroll
-                for (int bit = B0 + 3; bit < 5; ++bit) v[0] += __shfl_xor_sync(FULL, v[0], 1 << bit);
-                const int idx = (((lane >> B0) & 1) << 2) | (((lane >> (B0 + 1)) & 1) << 1) | ((lane >> (B0 + 2)) & 1);
-                if ((lane >> (B0 + 3)) == 0) sm.acc[(t * 2) * NP + SPT * g + idx] = v[0];
+                // the lane's dB partials replace the state after token t, which
+                // the walk no longer needs (token t+1 read it as its h_{t−1})
+                sm.Hs[(t * 2) * 32 + lane] = make_float4(v[0], v[1], v[2], v[3]);
+                sm.Hs[(t * 2 + 1) * 32 + lane] = make_float4(v[4], v[5], v[6], v[7]);
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) hcur[q] = hprev[q];
             }
+            __syncwarp();
+            // dB = Σ_c of the partials left in Hs
+            channel_sum(0, false);
             __syncwarp();
 
             // ---- the tile's dB, dC channel sums into memory (lane: one token,
