@@ -35,22 +35,50 @@ def stale(out: str = LIB) -> bool:
     return any(os.path.getmtime(p) > t for p in deps())
 
 
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC"]
+
+
 def nvcc_cmd(out: str, extra=()):
-    return (["nvcc", *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-             "-I", os.path.join(ROOT, "include"), *extra, "-o", out] + sources())
+    """One nvcc call that compiles every source straight into the library."""
+    return (["nvcc", *ARCH, *FLAGS, "-shared", "-I", os.path.join(ROOT, "include"), *extra, "-o", out]
+            + sources())
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    """Compile the library if any source is newer than it.  Returns its path."""
+def build(force: bool = False, verbose: bool = False, extra=(), jobs: int = 0) -> str:
+    """Compile the library if any source is newer than it.  Returns its path.
+
+    Each source compiles to its own object in a separate nvcc process (the
+    files share no device code, only inline header functions), in parallel,
+    and one nvcc call links them."""
     if not force and not stale():
         return LIB
+    from concurrent.futures import ThreadPoolExecutor
     os.makedirs(LIBDIR, exist_ok=True)
-    tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = nvcc_cmd(tmp, extra)
+    tag = "%d" % os.getpid()
+    objdir = os.path.join(LIBDIR, "obj." + tag)
+    os.makedirs(objdir, exist_ok=True)
+    inc = ["-I", os.path.join(ROOT, "include")]
+    srcs = sources()
+    objs = [os.path.join(objdir, os.path.basename(src) + ".o") for src in srcs]
+    cmds = [["nvcc", *ARCH, *FLAGS, *inc, *extra, "-c", src, "-o", obj] for src, obj in zip(srcs, objs)]
     if verbose:
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
+        for c in cmds:
+            print(" ".join(c), file=sys.stderr)
+    workers = jobs or min(len(cmds), os.cpu_count() or 1)
+    with ThreadPoolExecutor(workers) as ex:
+        results = list(ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), cmds))
+    for c, r in zip(cmds, results):
+        if r.returncode != 0:
+            sys.stderr.write(r.stdout + r.stderr)
+            raise subprocess.CalledProcessError(r.returncode, c)
+        if verbose and (r.stdout or r.stderr):
+            sys.stderr.write(r.stdout + r.stderr)
+    tmp = LIB + ".tmp" + tag
+    subprocess.run(["nvcc", *ARCH, "-shared", "-o", tmp, *objs], check=True)
     os.replace(tmp, LIB)
+    for o in objs:
+        os.remove(o)
+    os.rmdir(objdir)
     return LIB
 
 
