@@ -771,22 +771,27 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
     } else if (requested > 0) {
         p.chunk_len = std::min<int64_t>(requested, Lr);
     } else {
-        // Two-pass: pick the chunk length whose passes take the fewest rounds of
-        // resident warps × tokens per round.  A pass over n items takes
-        // ceil(n / resident) rounds of one chunk each; the aggregate pass costs
-        // about 0.7 of a main-pass chunk (no read-out, no output).  A single
-        // chunk (no aggregate pass) is one of the candidates.  Splitting adds
-        // two launches (aggregate, carry), charged as 64 tokens of one round.
+        // Two-pass: pick the chunk length with the least modelled time, in µs,
+        //   throughput:   all token-items of both passes (the aggregate pass
+        //                 costs ≈0.7 of the main one) spread over the resident
+        //                 warps, ≈0.1 µs per token per warp when they are all busy;
+        //   critical path: one chunk walked by one warp in both passes, ≈0.07 µs
+        //                 per token when few warps share an SM;
+        //   carry:        the carry pass steps through the K chunks, ≈1.1 µs each,
+        //                 and the two extra launches (≈8 µs).
+        // The constants are fits to B300 timings of the 2 × 1536 × 16 × 2048 and
+        // 1 × 5120 × 16 × 131072 layers over chunk lengths 64 .. 8192.  A single
+        // chunk (no aggregate pass) is one of the candidates.
         double best = 1e300;
         p.chunk_len = Lr;
         for (int64_t len = Lr; len >= 64; len -= 64) {
             const int64_t K = (seqlen + len - 1) / len;
             if (K > 64) break;
-            const int64_t rm = (p.groups * K + resident - 1) / resident;
-            const int64_t ra = (p.groups * (K - 1) + resident - 1) / resident;
-            const double cost = (double)len * ((double)rm + 0.7 * (double)ra) + (K > 1 ? 64.0 : 0.0);
-            if (cost < best * 0.999) {
-                best = cost;
+            const double items = (double)p.groups * ((double)K + 0.7 * (double)(K - 1)) * (double)len;
+            const double t = items * 0.1 / (double)resident + 1.7 * (double)len * 0.07 +
+                             (K > 1 ? 1.1 * (double)K + 8.0 : 0.0);
+            if (t < best * 0.999) {
+                best = t;
                 p.chunk_len = len;
             }
         }
