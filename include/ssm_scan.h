@@ -173,7 +173,7 @@ typedef struct {
     float *dh0;                           /* out: b × D × N fp32; NULL = not written */
     void *workspace;                      /* >= ssm_scan_bwd_workspace_size(...) bytes */
     size_t workspace_bytes;
-    int64_t chunk_len;                    /* 0 = automatic (256); else a multiple of 16 */
+    int64_t chunk_len;                    /* 0 = automatic (128); else a multiple of 16 */
 } ssm_scan_bwd_params;
 
 /* Bytes of workspace ssm_scan_bwd needs: the status word and work counters,

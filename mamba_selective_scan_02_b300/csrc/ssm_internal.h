@@ -118,7 +118,7 @@ cudaError_t ssd_launch(const SsdArgs &a, cudaStream_t stream);
 cudaError_t bwd_launch(const BwdArgs &a, bool bf16, cudaStream_t stream);
 int bwd_cpw(int64_t dstate);             // channels per warp of the backward kernels
 constexpr int kBwdTile = 16;             // tokens per checkpoint / recompute tile
-constexpr int kBwdChunk = 256;           // tokens per work item of the backward passes
+constexpr int kBwdChunk = 128;           // tokens per work item of the backward passes
 cudaError_t conv_step_launch(const ConvStepArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t mufu_ex2_launch(float *sink, int blocks, int iters, cudaStream_t stream);
 cudaError_t flag_wait_selftest_launch(int *status, const int *flag, int polls, cudaStream_t stream);
