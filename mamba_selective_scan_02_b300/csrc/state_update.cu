@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kStepThreads) step_wide_kernel(const StepArgs 
 // 16-byte word each, conflict-free), and the tile leaves with bulk stores.
 constexpr int kStreamCh = 128;     // channels per tile
 #ifndef SSM_STREAM_STAGES
-#define SSM_STREAM_STAGES 4
+#define SSM_STREAM_STAGES 3   // 3: 32.7 µs per token; 4: 33.6; 6: 38.1; 8: 44.3 (fewer CTAs fit)
 #endif
 constexpr int kStreamStages = SSM_STREAM_STAGES;  // stages in shared memory
 constexpr int kStreamAhead = kStreamStages - 2;   // tiles loading ahead of the one being updated
