@@ -623,20 +623,34 @@ __global__ void __launch_bounds__(256) widen_bc_kernel(const ScanArgs a) {
 
 // Chains the chunk aggregates from h0 (two-pass mode): carry[0] = h0 and
 // carry[k+1] = P_k · carry[k] + S_k, the state chunk k+1 starts from.
-// One thread per (b, d, n).
+// One thread per (b, d, n).  The aggregates do not depend on the chain, so they
+// are read kCarryBatch at a time before the chain steps through them: one L2
+// round trip per batch instead of one per chunk.
+constexpr int kCarryBatch = 16;
 __global__ void carry_kernel(const ScanArgs a) {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const size_t total = (size_t)a.batch * a.dim * a.dstate;
     if (i >= total) return;
-    const size_t bd = i / a.dstate;
-    const int n = (int)(i % a.dstate);
+    const size_t N = (size_t)a.dstate;
+    const size_t bd = i / N;
+    const int n = (int)(i % N);
     const int K = a.nchunks;
+    const float2 *__restrict__ agg = a.agg + bd * (K - 1) * N + n;
+    float *__restrict__ carry = a.carry + bd * K * N + n;
     float h = a.h0 ? a.h0[i] : 0.f;
-    a.carry[(bd * K) * a.dstate + n] = h;
-    for (int k = 0; k + 1 < K; ++k) {
-        const float2 ps = a.agg[(bd * (K - 1) + k) * a.dstate + n];
-        h = fmaf(ps.x, h, ps.y);
-        a.carry[(bd * K + k + 1) * a.dstate + n] = h;
+    carry[0] = h;
+    for (int k0 = 0; k0 + 1 < K; k0 += kCarryBatch) {
+        float2 ps[kCarryBatch];
+#pragma unroll
+        for (int j = 0; j < kCarryBatch; ++j)
+            ps[j] = (k0 + j + 1 < K) ? agg[(size_t)(k0 + j) * N] : make_float2(1.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < kCarryBatch; ++j) {
+            if (k0 + j + 1 < K) {
+                h = fmaf(ps[j].x, h, ps[j].y);
+                carry[(size_t)(k0 + j + 1) * N] = h;
+            }
+        }
     }
 }
 
