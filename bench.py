@@ -92,7 +92,7 @@ def weak_scaling_value(elems_per_rank: float, world: int, ms_max: float) -> floa
 # ------------------------------------------------------------------ ncu record
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
-    "scan_kernel": ["scan_fwd.cu", "ssm_device.cuh", "ssm_internal.h"],
+    "scan_ws_kernel": ["scan_fwd.cu", "ssm_device.cuh", "ssm_internal.h"],
     "step_stream_kernel": ["state_update.cu", "ssm_device.cuh", "ssm_internal.h"],
     "conv1d_stream_kernel": ["conv1d.cu", "ssm_device.cuh", "ssm_internal.h"],
     "conv1d_step8_kernel": ["conv1d.cu", "ssm_device.cuh", "ssm_internal.h"],
@@ -384,7 +384,7 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {
             "bound": "alu", "unit": "Gex2/s", "achieved": achieved_ex2, "peak": mufu_peak,
-            "frac": achieved_ex2 / mufu_peak, "traffic": recorded_traffic("scan_kernel"),
+            "frac": achieved_ex2 / mufu_peak, "traffic": recorded_traffic("scan_ws_kernel"),
             "peak_source": "MUFU ex2.approx throughput measured in this run (ssm_bench_mufu_ex2)",
             "kernel_ms": kern_ms,
             "hbm": {"achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
