@@ -892,7 +892,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 failed = true;
                 break;
             }
-#pragma unroll 1
+#pragma unroll 2
             for (int lb = 0; lb < 2; ++lb) {
                 const int blk = 2 * hh + lb;
                 const float4 *dd = terms_of(hh, 0) + c * TP + 4 * lb;
@@ -936,15 +936,14 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 float p[8];
                 float2 hp[NQ];
                 auto readout = [&](int j, const float2 *hs, const float4 *cr) {
-                    float2 acc0 = mul2(make_float2(cr[0].x, cr[0].y), hs[0]);
-                    float2 acc1 = mul2(make_float2(cr[0].z, cr[0].w), hs[1]);
+                    float2 acc = mul2(make_float2(cr[0].x, cr[0].y), hs[0]);
+                    acc = fma2(make_float2(cr[0].z, cr[0].w), hs[1], acc);
 #pragma unroll
                     for (int q4 = 1; q4 < NR; ++q4) {
-                        acc0 = fma2(make_float2(cr[q4].x, cr[q4].y), hs[2 * q4], acc0);
-                        acc1 = fma2(make_float2(cr[q4].z, cr[q4].w), hs[2 * q4 + 1], acc1);
+                        acc = fma2(make_float2(cr[q4].x, cr[q4].y), hs[2 * q4], acc);
+                        acc = fma2(make_float2(cr[q4].z, cr[q4].w), hs[2 * q4 + 1], acc);
                     }
-                    const float2 s2 = add2(acc0, acc1);
-                    p[j] = s2.x + s2.y;
+                    p[j] = acc.x + acc.y;
                 };
                 float4 Bnx[NR], Cnx[NR];
                 {
