@@ -122,7 +122,7 @@ def test_workspace_size():
 
 def test_scan_plan():
     plan = capi.ssm_scan_plan(valid_scan(batch=4, dim=5120, seqlen=2048))
-    assert plan == {"chunk_len": 256, "nchunks": 8, "chained": True, "groups": 1280}
+    assert plan == {"chunk_len": 384, "nchunks": 6, "chained": True, "groups": 1280}
     plan = capi.ssm_scan_plan(valid_scan(batch=1, dim=5120, seqlen=131072))
     assert not plan["chained"] and plan["nchunks"] > 1 and plan["chunk_len"] % 64 == 0
     plan = capi.ssm_scan_plan(valid_scan(batch=1, dim=64, seqlen=64))
