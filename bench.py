@@ -537,8 +537,8 @@ def run_ours(args):
                     dA=torch.empty((w.dim, w.dstate), dtype=torch.float32, device=dev),
                     dD=torch.empty(w.dim, dtype=torch.float32, device=dev),
                     ddelta_bias=torch.empty(w.dim, dtype=torch.float32, device=dev))
-        bws = torch.empty(api.bwd_workspace_bytes(bb, w.dim, w.dstate, w.seqlen), dtype=torch.uint8,
-                          device=dev)
+        bws = torch.empty(api.bwd_workspace_bytes(bb, w.dim, w.dstate, w.seqlen, dtype=bi["u"].dtype),
+                          dtype=torch.uint8, device=dev)
         bp = api.bwd_params(bi["u"], bi["delta"], bi["A"], bi["B"], bi["C"], dy, bi["Dskip"], bi["z"],
                             bi["bias"], None, None, workspace=bws, **bout)
         for _ in range(3):

@@ -176,15 +176,23 @@ typedef struct {
     int64_t chunk_len;                    /* 0 = automatic (128); else a multiple of 16 */
 } ssm_scan_bwd_params;
 
-/* Bytes of workspace ssm_scan_bwd needs: the status word and work counters,
- * two chained hand-off states of b × D × N fp32, and the recurrence state at
- * every 16th token (4 bytes per (b, d, t) element for N = 16).  0 for invalid
- * sizes. */
+/* Bytes of workspace ssm_scan_bwd needs for the sizes, io_dtype, zoh and
+ * chunk_len in *p (the pointers are not read): the status word and work
+ * counters, two chained hand-off states of b × D × N fp32, and the recurrence
+ * state at every 16th token (4 bytes per (b, d, t) element for N = 16).  With
+ * bf16 I/O, first order, 9 <= N <= 16 and enough channel groups for a chained
+ * forward plan, the checkpoints come from the forward scan kernel, which adds
+ * its flags, one more b × D × N hand-off state and B, C as fp32 rows
+ * (2 × b × L × 16 × 4 bytes); a workspace without that room still works,
+ * with the backward's own checkpoint pass.  0 for invalid sizes. */
 size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params *p);
 
-/* The backward scan: two launches on `stream` (a checkpoint pass and the
- * reverse pass) after clearing the accumulated outputs.  Device-side wait
- * failures are reported through ssm_workspace_status on this workspace. */
+/* The backward scan on `stream`, after clearing the accumulated outputs: a
+ * checkpoint pass (the forward recurrence, writing the state at every 16th
+ * token — on the forward scan's warp-specialised kernel where the workspace
+ * size above includes its room, else on a kernel of its own) and the reverse
+ * pass.  Device-side wait failures are reported through ssm_workspace_status
+ * on this workspace. */
 ssm_status ssm_scan_bwd(const ssm_scan_bwd_params *p, ssm_stream_t stream);
 
 /* ------------------------------------------------------------------------

@@ -184,10 +184,16 @@ def bwd_params(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, h0=None, 
     return p
 
 
-def bwd_workspace_bytes(batch, dim, dstate, seqlen, chunk_len=0) -> int:
+def bwd_workspace_bytes(batch, dim, dstate, seqlen, chunk_len=0, dtype=torch.bfloat16, zoh=False) -> int:
+    """Workspace bytes of ssm_scan_bwd.  The I/O dtype and the discretisation
+    matter: bf16 first-order backward passes with enough channel groups take
+    their state checkpoints from the forward scan kernel, which needs room of
+    its own."""
     p = capi.BwdParams()
     p.batch, p.dim, p.dstate, p.seqlen = batch, dim, dstate, seqlen
     p.chunk_len = int(chunk_len)
+    p.io_dtype = _DT[dtype]
+    p.zoh = int(bool(zoh))
     n = capi.ssm_scan_bwd_workspace_size(p)
     if n == 0:
         raise ValueError("invalid backward scan sizes")
@@ -212,7 +218,8 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, h0=None, dh
                ddelta_bias=torch.empty(dim, dtype=f32, device=dev) if delta_bias is not None else None,
                dh0=torch.empty((b, dim, N), dtype=f32, device=dev) if h0 is not None else None)
     if workspace is None:
-        workspace = torch.empty(bwd_workspace_bytes(b, dim, N, L, chunk_len), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(bwd_workspace_bytes(b, dim, N, L, chunk_len, u.dtype, zoh), dtype=torch.uint8,
+                                device=dev)
     p = bwd_params(u, delta, A, B, C, dy, D, z, delta_bias, h0, dhL, du=out["du"], ddelta=out["ddelta"],
                    dB=out["dB"], dC=out["dC"], dA=out["dA"], dz=out["dz"], dD=out["dD"],
                    ddelta_bias=out["ddelta_bias"], dh0=out["dh0"], delta_softplus=delta_softplus, zoh=zoh,

@@ -75,12 +75,20 @@ bool bwd_sizes_ok(const ssm_scan_bwd_params *p) {
 struct BwdLayout {
     int64_t groups, ntiles, chunk_len, nchunks;
     size_t flags_fwd, flags_rev, carry_fwd, carry_rev, ckpt, zero_bytes, total;
+    // the checkpoint pass on the forward scan kernel (when scan_ckpt_supported)
+    bool scan_ckpt;
+    ssm::ScanPlan plan;
+    size_t scan_flags, scan_carry, scan_bt, scan_ct;
+    size_t own_total;  // the workspace the backward's own checkpoint pass needs
 };
 
-// Backward workspace: the 256-byte header (status word, two work counters),
-// one int flag per channel group for each pass, the two b × D × N fp32
-// hand-off states, then the state at every tile start, [group][tile][256]
-// fp32.  The header and the flags are cleared before every call.
+// Backward workspace: the 256-byte header (status word, two work counters of
+// the backward passes, two of the forward kernel's checkpoint launch), one int
+// flag per channel group for each pass (and for the checkpoint launch), the two
+// b × D × N fp32 hand-off states, the state at every tile start,
+// [group][tile][256] fp32, and for the checkpoint launch its own hand-off
+// state and B, C widened to fp32.  The header and the flags are cleared before
+// every call.
 BwdLayout bwd_layout(const ssm_scan_bwd_params *p) {
     BwdLayout l;
     const int cpw = ssm::bwd_cpw(p->dstate);
@@ -88,6 +96,9 @@ BwdLayout bwd_layout(const ssm_scan_bwd_params *p) {
     l.ntiles = (p->seqlen + ssm::kBwdTile - 1) / ssm::kBwdTile;
     l.chunk_len = p->chunk_len > 0 ? p->chunk_len : ssm::kBwdChunk;
     l.nchunks = (p->seqlen + l.chunk_len - 1) / l.chunk_len;
+    l.plan = ssm::scan_plan(p->batch, p->dim, p->dstate, p->seqlen, 0);
+    l.scan_ckpt = ssm::scan_ckpt_supported(l.plan, p->dstate, p->seqlen, p->io_dtype == SSM_BF16, p->zoh) &&
+                  l.plan.groups == l.groups;
     const size_t flag_bytes = align256((size_t)l.groups * sizeof(int));
     const size_t bdn = align256((size_t)p->batch * p->dim * p->dstate * sizeof(float));
     l.flags_fwd = kHeader;
@@ -97,6 +108,16 @@ BwdLayout bwd_layout(const ssm_scan_bwd_params *p) {
     l.carry_rev = l.carry_fwd + bdn;
     l.ckpt = l.carry_rev + bdn;
     l.total = l.ckpt + (size_t)l.groups * l.ntiles * 256 * sizeof(float);
+    l.own_total = l.total;
+    l.scan_flags = l.scan_carry = l.scan_bt = l.scan_ct = l.total;
+    if (l.scan_ckpt) {  // after the backward's own regions, cleared separately
+        const size_t bt = align256((size_t)p->batch * p->seqlen * l.plan.np * sizeof(float));
+        l.scan_flags = l.total;
+        l.scan_carry = l.scan_flags + flag_bytes;
+        l.scan_bt = l.scan_carry + bdn;
+        l.scan_ct = l.scan_bt + bt;
+        l.total = l.scan_ct + bt;
+    }
     return l;
 }
 
@@ -142,7 +163,10 @@ ssm_status ssm_scan_bwd(const ssm_scan_bwd_params *p, ssm_stream_t stream) {
         overlaps(p->dC, bcf, p->C, bc))
         return SSM_ERR_INVALID_ARG;
     const BwdLayout l = bwd_layout(p);
-    if (p->workspace_bytes < l.total) return SSM_ERR_INVALID_ARG;
+    // A workspace without room for the forward kernel's checkpoint launch still
+    // runs, with the backward's own checkpoint pass.
+    if (p->workspace_bytes < l.own_total) return SSM_ERR_INVALID_ARG;
+    const bool scan_ckpt = l.scan_ckpt && p->workspace_bytes >= l.total;
     if (l.groups * l.nchunks > INT32_MAX / 2 || l.groups * l.ntiles > INT32_MAX / 2) return SSM_ERR_UNSUPPORTED;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -194,6 +218,41 @@ ssm_status ssm_scan_bwd(const ssm_scan_bwd_params *p, ssm_stream_t stream) {
     a.nchunks = (int)l.nchunks;
     a.groups = (int)l.groups;
     a.ntiles = (int)l.ntiles;
+    a.ckpt_ready = 0;
+    if (scan_ckpt && aligned16(p->u) && aligned16(p->delta)) {
+        // The checkpoint pass as the forward scan's warp-specialised kernel.
+        if (cudaMemsetAsync(ws + l.scan_flags, 0, (size_t)l.groups * sizeof(int), st) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        ssm::ScanArgs f;
+        memset(&f, 0, sizeof(f));
+        f.batch = a.batch;
+        f.dim = a.dim;
+        f.dstate = a.dstate;
+        f.seqlen = a.seqlen;
+        f.u = p->u;
+        f.delta = p->delta;
+        f.B = p->B;
+        f.C = p->C;
+        f.A = p->A;
+        f.bias = p->delta_bias;
+        f.delta_softplus = p->delta_softplus;
+        f.h0 = p->h0;
+        f.status = a.status;
+        f.tickets = reinterpret_cast<int *>(ws) + 4;
+        f.flags = reinterpret_cast<int *>(ws + l.scan_flags);
+        f.carry = reinterpret_cast<float *>(ws + l.scan_carry);
+        f.chunk_len = (int)l.plan.chunk_len;
+        f.nchunks = (int)l.plan.nchunks;
+        f.groups = (int)l.plan.groups;
+        f.chained = 1;
+        f.Bt = reinterpret_cast<float *>(ws + l.scan_bt);
+        f.Ct = reinterpret_cast<float *>(ws + l.scan_ct);
+        f.np = l.plan.np;
+        f.ckpt = a.ckpt;
+        f.ckpt_tiles = a.ntiles;
+        if (ssm::scan_ckpt_launch(f, st) != cudaSuccess) return SSM_ERR_CUDA;
+        a.ckpt_ready = 1;
+    }
     return ssm::bwd_launch(a, p->io_dtype == SSM_BF16, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -269,6 +328,8 @@ ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream) {
     a.Bt = reinterpret_cast<float *>(ws + l.bt_off);
     a.Ct = reinterpret_cast<float *>(ws + l.ct_off);
     a.np = l.plan.np;
+    a.ckpt = nullptr;
+    a.ckpt_tiles = 0;
     return ssm::scan_launch(a, p->io_dtype == SSM_BF16, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

@@ -636,13 +636,16 @@ int resident_warps(const void *kern, size_t smem) {
 template <typename T, int NG, bool HAS_Z, bool ZOH, bool VEC>
 cudaError_t launch_pair(const BwdArgs &a, cudaStream_t st) {
     const int items = a.groups * a.nchunks;
-    auto k1 = bwd_ckpt_kernel<T, NG, ZOH, VEC>;
-    static int res1 = 0;
-    if (res1 == 0) res1 = resident_warps(reinterpret_cast<const void *>(k1), 0);
-    if (res1 == 0) return cudaErrorInvalidConfiguration;
-    k1<<<std::max(1, std::min(items, res1)), 32, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (!a.ckpt_ready) {
+        auto k1 = bwd_ckpt_kernel<T, NG, ZOH, VEC>;
+        static int res1 = 0;
+        if (res1 == 0) res1 = resident_warps(reinterpret_cast<const void *>(k1), 0);
+        if (res1 == 0) return cudaErrorInvalidConfiguration;
+        k1<<<std::max(1, std::min(items, res1)), 32, 0, st>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
 
     auto k2 = bwd_rev_kernel<T, NG, HAS_Z, ZOH, VEC>;
     constexpr size_t smem = sizeof(RevSmem<NG>);

@@ -649,7 +649,9 @@ template <typename T> struct WsTile {
 
 constexpr int kWsFirst = 1, kWsLast = 2, kWsEnd = 4;  // header flags
 
-template <typename T, bool HAS_Z, bool ZOH>
+// CK: the backward's checkpoint pass — the state at every 16-token tile start
+// into a.ckpt, no read-out, no y, no C.
+template <typename T, bool HAS_Z, bool ZOH, bool CK>
 __global__ void __launch_bounds__(256, 2)
 scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     using S = WsTile<T>;
@@ -706,7 +708,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
         auto issue = [&](const Item &it, int tile, int s) {  // lane 0
             const int t0 = it.t_begin + tile * kTT;
             unsigned char *st = stage(s);
-            mbar_arrive_expect_tx(&tma_full[s], (HAS_Z ? 3u : 2u) * Wt::SEQ + 2u * Wt::BC);
+            mbar_arrive_expect_tx(&tma_full[s], (HAS_Z ? 3u : 2u) * Wt::SEQ + (CK ? 1u : 2u) * Wt::BC);
 #pragma unroll
             for (int j = 0; j < NB8; ++j) {
                 tma_load_3d(st + Wt::off_u + j * Wt::BLK, &maps.u, &tma_full[s], t0 + 8 * j, it.d0, it.b);
@@ -714,7 +716,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 if (HAS_Z) tma_load_3d(st + Wt::off_z + j * Wt::BLK, &maps.z, &tma_full[s], t0 + 8 * j, it.d0, it.b);
             }
             tma_load_3d(st + Wt::off_B, &maps.B, &tma_full[s], 0, t0, it.b);
-            tma_load_3d(st + Wt::off_C, &maps.C, &tma_full[s], 0, t0, it.b);
+            if (!CK) tma_load_3d(st + Wt::off_C, &maps.C, &tma_full[s], 0, t0, it.b);
         };
         bool ok = true;
         // Publishes the end of the work in slot 0 after `tiles` tiles went out.
@@ -778,10 +780,12 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     if (2 * j + 1 >= valid) x.y = 0.f;
                     const float2 uu = make_float2(uf[2 * j], uf[2 * j + 1]);
                     const float2 du = mul2(x, uu);
-                    const float2 gt = HAS_Z ? gate2<T>(make_float2(zf[2 * j], zf[2 * j + 1])) : make_float2(1.f, 1.f);
-                    const float2 dg = mul2(mul2(make_float2(skip, skip), uu), gt);
                     dd[j] = make_float4(x.x, x.y, du.x, du.y);
-                    gd[j] = make_float4(gt.x, gt.y, dg.x, dg.y);
+                    if (!CK) {
+                        const float2 gt = HAS_Z ? gate2<T>(make_float2(zf[2 * j], zf[2 * j + 1])) : make_float2(1.f, 1.f);
+                        const float2 dg = mul2(mul2(make_float2(skip, skip), uu), gt);
+                        gd[j] = make_float4(gt.x, gt.y, dg.x, dg.y);
+                    }
                 }
                 if (lane == 0) hdr[h] = make_int4(cur, tile, flags, 0);
                 __syncwarp();
@@ -882,7 +886,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             break;
         }
         // The y tile written two tiles ago must have left shared memory.
-        if (lane == 0) bulk_wait_read1();
+        if (!CK && lane == 0) bulk_wait_read1();
         __syncwarp();
         const int t0 = it.t_begin + tile * kTT;
         const unsigned char *st = stage(s);
@@ -894,6 +898,14 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             if (hh == 1 && !ws_wait(&trm_full[1], i & 1)) {
                 failed = true;
                 break;
+            }
+            if (CK) {  // the state entering this 16-token tile is its checkpoint
+                const int tk = t0 + 16 * hh;
+                if (tk < L) {
+                    float4 *ck = reinterpret_cast<float4 *>(a.ckpt) + ((size_t)it.grp * a.ckpt_tiles + tk / 16) * 64;
+                    ck[lane] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+                    ck[32 + lane] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
+                }
             }
 #pragma unroll 2
             for (int lb = 0; lb < 2; ++lb) {
@@ -972,11 +984,14 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     }
 #pragma unroll
                     for (int q = 0; q < NQ; ++q) h[q] = fma2(ac[q], h[q], bc[q]);
-                    if (j > 0) readout(j - 1, hp, Cnx);
-                    load_row(Cf, j, Cnx);
+                    if (!CK) {
+                        if (j > 0) readout(j - 1, hp, Cnx);
+                        load_row(Cf, j, Cnx);
 #pragma unroll
-                    for (int q = 0; q < NQ; ++q) hp[q] = h[q];
+                        for (int q = 0; q < NQ; ++q) hp[q] = h[q];
+                    }
                 }
+                if (CK) continue;
                 readout(7, hp, Cnx);
                 // Transposed sum over the two lanes of a channel: lane g keeps
                 // tokens 4g .. 4g+3, whose gate terms sit in pairs 2g, 2g+1.
@@ -996,21 +1011,23 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             ws_arrive(&trm_empty[hh]);  // this half's terms are read
         }
         if (failed) break;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+        if (!CK) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
 #pragma unroll
-            for (int j = 0; j < NB8; ++j) tma_store_3d(&maps.y, out + j * (CPW * 8), t0 + 8 * j, it.d0, it.b);
-            bulk_commit();
+                for (int j = 0; j < NB8; ++j) tma_store_3d(&maps.y, out + j * (CPW * 8), t0 + 8 * j, it.d0, it.b);
+                bulk_commit();
+            }
+            ostage ^= 1;
         }
-        ostage ^= 1;
         __syncwarp();
         ws_arrive(&stage_empty[s]);  // this tile's B, C rows are read
         if (hd.z & kWsLast) {
             // ---- item end: hand the state on, or write the final state
             float *dst = nullptr;
             const bool last = it.k == K - 1;
-            if (last) dst = a.hL ? a.hL + ((size_t)it.b * D + d) * N : nullptr;
+            if (last) dst = (!CK && a.hL) ? a.hL + ((size_t)it.b * D + d) * N : nullptr;
             else if (chained) dst = a.carry + ((size_t)it.b * D + d) * N;
             if (dst && live) {
 #pragma unroll
@@ -1029,7 +1046,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
         }
     }
     if (failed) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
-    if (lane == 0) bulk_wait0();
+    if (!CK && lane == 0) bulk_wait0();
 }
 
 // B and C, [b][N][L] in the I/O type, widened once per launch to fp32
@@ -1156,10 +1173,10 @@ cudaError_t launch_one(const Maps &maps, const ScanArgs &a, int items, cudaStrea
     return cudaGetLastError();
 }
 
-template <typename T, bool HAS_Z, bool ZOH>
+template <typename T, bool HAS_Z, bool ZOH, bool CK = false>
 cudaError_t launch_ws(const Maps &maps, const ScanArgs &a, int items, cudaStream_t st) {
     using S = WsTile<T>;
-    auto kern = scan_ws_kernel<T, HAS_Z, ZOH>;
+    auto kern = scan_ws_kernel<T, HAS_Z, ZOH, CK>;
     static int per_sm = 0;  // resident CTAs (four consumer warps each) per SM
     if (per_sm == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::bytes);
@@ -1272,6 +1289,27 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
     p.nchunks = (seqlen + p.chunk_len - 1) / p.chunk_len;
     if (p.nchunks == 1) p.chained = false;
     return p;
+}
+
+bool scan_ckpt_supported(const ScanPlan &plan, int64_t dstate, int64_t seqlen, bool bf16, int zoh) {
+    const Split sp = split_for(dstate);
+    return SSM_SCAN_WS && bf16 && zoh == 0 && sp.spt == 8 && sp.ng == 2 && plan.chained && (seqlen * 2) % 16 == 0;
+}
+
+cudaError_t scan_ckpt_launch(const ScanArgs &a, cudaStream_t st) {
+    using T = __nv_bfloat16;
+    const int cpw = 16;
+    Maps maps;
+    memset(&maps, 0, sizeof(maps));
+    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const bool ok = make_map(&maps.u, dt, 2, a.u, a.seqlen, a.dim, a.batch, 8, cpw) &&
+                    make_map(&maps.d, dt, 2, a.delta, a.seqlen, a.dim, a.batch, 8, cpw) &&
+                    make_map(&maps.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.Bt, a.np, a.seqlen, a.batch, a.np, kTT);
+    if (!ok || !a.ckpt || !a.chained) return cudaErrorInvalidValue;
+    widen_bc_kernel<T><<<dim3((a.seqlen + 31) / 32, a.batch), 256, 0, st>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_ws<T, false, false, true>(maps, a, a.groups * a.nchunks, st);
 }
 
 cudaError_t scan_launch(const ScanArgs &a, bool bf16, cudaStream_t st) {

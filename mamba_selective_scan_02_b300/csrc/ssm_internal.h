@@ -27,6 +27,8 @@ struct ScanArgs {
     int chained;     // 1: chunk k waits for chunk k-1's state; 0: two-pass carries
     float *Bt, *Ct;  // B and C widened to fp32, token-major: [b][L][np], zero beyond N
     int np;          // states per token row of Bt / Ct (N rounded up to 4, 8 or 16)
+    float *ckpt;     // checkpoint launch only: the state at every 16-token tile start,
+    int ckpt_tiles;  // [group][tile][2][32 lanes] float4 as the backward's reverse pass reads it
 };
 
 // How a scan is cut into work items.  One warp owns a group of channels for
@@ -71,6 +73,7 @@ struct BwdArgs {
     float *carry_fwd, *carry_rev;    // b × D × N hand-offs: the state forward, the adjoint backward
     float *ckpt;                     // [group][tile][2][32 lanes] float4: the state at every tile start
     int chunk_len, nchunks, groups, ntiles;
+    int ckpt_ready;                  // 1: the forward scan already wrote ckpt (no checkpoint pass)
 };
 
 // Mamba-2 (SSD) layer: heads of P channels with a scalar A each.
@@ -111,6 +114,11 @@ struct ConvStepArgs {
 int scan_groups(int64_t dstate);
 ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t requested);
 cudaError_t scan_launch(const ScanArgs &a, bool bf16, cudaStream_t stream);
+// The backward's checkpoint pass on the forward's warp-specialised kernel: no y,
+// the state at every 16-token tile start into a.ckpt.  Supported for bf16 I/O,
+// first order, 9 <= N <= 16, a row pitch TMA can describe and a chained plan.
+bool scan_ckpt_supported(const ScanPlan &plan, int64_t dstate, int64_t seqlen, bool bf16, int zoh);
+cudaError_t scan_ckpt_launch(const ScanArgs &a, cudaStream_t stream);
 cudaError_t step_launch(const StepArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t conv_launch(const ConvArgs &a, bool bf16, cudaStream_t stream);
 bool ssd_supported(int64_t headdim, int64_t dstate);

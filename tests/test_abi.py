@@ -280,6 +280,22 @@ def test_bwd_workspace_size():
     assert capi.lib().ssm_scan_bwd(None, None) == capi.SSM_ERR_INVALID_ARG
 
 
+def test_bwd_workspace_size_with_forward_checkpoints():
+    # Enough channel groups for a chained forward plan (bf16, first order): the
+    # checkpoint pass runs on the forward scan kernel, which adds its own flags,
+    # hand-off state and fp32 B, C rows to the workspace.
+    b, d, n, L = 4, 5120, 16, 2048
+    groups, ntiles = b * d // 16, L // 16
+    flags = -(-groups * 4 // 256) * 256
+    bdn = -(-b * d * n * 4 // 256) * 256
+    bt = -(-b * L * 16 * 4 // 256) * 256
+    base = 256 + 2 * flags + 2 * bdn + groups * ntiles * 1024
+    p = valid_bwd(batch=b, dim=d, seqlen=L)
+    assert capi.ssm_scan_bwd_workspace_size(p) == base + flags + bdn + 2 * bt
+    # the zero-order hold keeps the backward's own checkpoint pass
+    assert capi.ssm_scan_bwd_workspace_size(valid_bwd(batch=b, dim=d, seqlen=L, zoh=1)) == base
+
+
 def valid_ssd(**over):
     p = capi.SsdParams()
     p.batch, p.seqlen, p.nheads, p.headdim, p.dstate = 2, 256, 4, 64, 128

@@ -110,20 +110,23 @@ def test_bwd_without_optional_inputs():
     assert out["dD"] is None and out["ddelta_bias"] is None and out["dh0"] is None
 
 
-@pytest.mark.gpu
-def test_bwd_mamba28b_layer_sampled():
-    # the layer shape the forward is measured on, in the launch configuration the
-    # benchmark times (chunks of 256 tokens, chained both ways): per-channel
-    # gradients on sampled channels, the per-channel sums over the batch for
-    # those channels, and dB, dC of the first sequence over all 5120 channels
-    b, D, N, L = 4, 5120, 16, 2048
-    inp = draw("bf16", b, D, N, L, seed=2)
+def sampled_check(b, D, N, L, seed, nchan=12, own_checkpoints=False):
+    """Per-channel gradients on sampled channels, the per-channel sums over the
+    batch for those channels, and dB, dC of the first sequence over all D
+    channels, against the oracle.  own_checkpoints: a workspace with no room
+    for the forward kernel's checkpoint launch (the backward's own pass runs)."""
+    inp = draw("bf16", b, D, N, L, seed=seed)
+    ws = None
+    if own_checkpoints:
+        small = api.bwd_workspace_bytes(b, D, N, L, dtype=torch.float32)
+        assert small < api.bwd_workspace_bytes(b, D, N, L, dtype=torch.bfloat16)
+        ws = torch.empty(small, dtype=torch.uint8, device="cuda")
     out = api.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["dy"], inp["D"], inp["z"],
-                       inp["bias"], inp["h0"], inp["dhL"])
+                       inp["bias"], inp["h0"], inp["dhL"], workspace=ws)
     torch.cuda.synchronize()
     assert api.workspace_status(out["workspace"]) == 0
     dtype = torch.bfloat16
-    chans = sorted({d for _, d in tu.sample_channels(b, D, 12, seed=4)})
+    chans = sorted({d for _, d in tu.sample_channels(b, D, nchan, seed=seed + 2)})
     for d in chans:
         sl = lambda t: None if t is None else t[:, d:d + 1].cpu()
         want = orc.scan_bwd(sl(inp["u"]), sl(inp["delta"]), inp["A"][d:d + 1].cpu(), inp["B"].cpu(),
@@ -140,3 +143,21 @@ def test_bwd_mamba28b_layer_sampled():
                         h0=b0(inp["h0"]), dhL=b0(inp["dhL"]), threads=16)
     check("dB[0]", out["dB"][0:1], want["dB"], dtype)
     check("dC[0]", out["dC"][0:1], want["dC"], dtype)
+
+
+@pytest.mark.gpu
+def test_bwd_mamba28b_layer_sampled():
+    # The layer shape the forward is measured on, in the launch configuration
+    # the benchmark times: the state checkpoints come from the forward scan's
+    # warp-specialised kernel (a chained plan of 384-token chunks), the reverse
+    # pass walks 128-token chunks.
+    sampled_check(4, 5120, 16, 2048, seed=2)
+
+
+@pytest.mark.gpu
+def test_bwd_forward_checkpoints_ragged():
+    # Enough channel groups (896) for the forward kernel's checkpoint launch, on
+    # a sequence of two chained chunks whose last 32-token tile holds 8 tokens.
+    sampled_check(2, 7168, 16, 456, seed=5, nchan=8)
+    # the same shape with the backward's own checkpoint pass
+    sampled_check(2, 7168, 16, 456, seed=5, nchan=8, own_checkpoints=True)
