@@ -61,12 +61,27 @@ def test_small_shapes(b, D, N, L, dtype, opts):
 
 def test_chained_chunks_every_element():
     """Enough channel groups that chunk k starts from the state chunk k-1 hands
-    over (one warp per 16 channels; 3,600 channels leave a partial group)."""
+    over (one warp per 16 channels: 225 groups per sequence)."""
     inp = _case(4, 3600, 16, 512, torch.bfloat16, seed=21, h0=True)
     p = capi.ScanParams()
     p.batch, p.dim, p.dstate, p.seqlen, p.chunk_len = 4, 3600, 16, 512, 64
     assert capi.ssm_scan_plan(p)["chained"]
     _check(inp, torch.bfloat16, "chained 4x3600x16x512", chunk_len=64)
+
+
+@pytest.mark.parametrize("chunk", [64, 0])
+def test_chained_ragged_every_element(chunk):
+    """The warp-specialised pass in chained mode on a ragged layer: 3,608
+    channels (a partial 16-channel group per sequence), 456 tokens (the last
+    32-token tile holds 8), with h0 and no gate; chunks of 64 tokens (eight
+    hand-offs per group) or the default length (two)."""
+    b, D, N, L = 4, 3608, 16, 456
+    inp = _case(b, D, N, L, torch.bfloat16, seed=23, z=False, h0=True)
+    p = capi.ScanParams()
+    p.batch, p.dim, p.dstate, p.seqlen, p.chunk_len = b, D, N, L, chunk
+    plan = capi.ssm_scan_plan(p)
+    assert plan["chained"] and plan["groups"] == b * 226 and plan["nchunks"] == (8 if chunk else 2)
+    _check(inp, torch.bfloat16, f"chained ragged {b}x{D}x{N}x{L} chunk {chunk}", chunk_len=chunk)
 
 
 def test_small_layer_workload_full():
