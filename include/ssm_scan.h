@@ -105,7 +105,11 @@ size_t ssm_scan_workspace_size(const ssm_scan_params *p);
 ssm_status ssm_scan_plan(const ssm_scan_params *p, int64_t out[4]);
 
 /* Forward selective scan: writes y and (if non-NULL) hL.  Also clears the
- * workspace status word before launching. */
+ * workspace status word before launching.  In chained mode the launch's warps
+ * wait on one another (bounded spins on flags in the workspace); its grid is
+ * sized to the CTAs the device holds at once, so work that occupies SMs for
+ * long on another stream can delay it, and a wait that reaches its bound is
+ * reported as SSM_ERR_TIMEOUT through ssm_workspace_status. */
 ssm_status ssm_scan_fwd(const ssm_scan_params *p, ssm_stream_t stream);
 
 typedef struct {
