@@ -649,11 +649,15 @@ template <typename T> struct WsTile {
 
 constexpr int kWsFirst = 1, kWsLast = 2, kWsEnd = 4;  // header flags
 
-// CK: the backward's checkpoint pass — the state at every 16-token tile start
-// into a.ckpt, no read-out, no y, no C.
-template <typename T, bool HAS_Z, bool ZOH, bool CK>
+// WM = 0: the main pass (y, and hL or the hand-off after each item).
+// WM = 1: the two-pass aggregate pass — each chunk but the last from a zero
+//         state, (Π Ā, h_end) into a.agg; no read-out, no y, no C.
+// WM = 2: the backward's checkpoint pass — the state at every 16-token tile
+//         start into a.ckpt; no read-out, no y, no C.
+template <typename T, bool HAS_Z, bool ZOH, int WM>
 __global__ void __launch_bounds__(256, 2)
 scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
+    constexpr bool OUTY = WM == 0, AG = WM == 1, CK = WM == 2;
     using S = WsTile<T>;
     using Wt = WTile<T, 8, 2>;
     constexpr int SPT = 8, CPW = Wt::CPW, NB8 = Wt::NB8, NQ = SPT / 2, NR = SPT / 4, TP = S::TP;
@@ -670,7 +674,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     int4 *hdr = reinterpret_cast<int4 *>(smem + S::off_hdr);
     const int D = a.dim, N = a.dstate, L = a.seqlen, K = a.nchunks;
     const int gpb = (D + CPW - 1) / CPW;
-    const int items = a.groups * K;
+    const int items = a.groups * (AG ? K - 1 : K);
     const bool chained = a.chained;
 
     auto item_of = [&](int t) {
@@ -702,13 +706,13 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
         const int c = lane >> 1, hg = lane & 1;  // channel, which 8-token block of a half tile
         auto grab = [&]() {
             int t = 0;
-            if (lane == 0) t = atomicAdd(a.tickets, 1);
+            if (lane == 0) t = atomicAdd(a.tickets + (AG ? 1 : 0), 1);
             return __shfl_sync(FULL, t, 0);
         };
         auto issue = [&](const Item &it, int tile, int s) {  // lane 0
             const int t0 = it.t_begin + tile * kTT;
             unsigned char *st = stage(s);
-            mbar_arrive_expect_tx(&tma_full[s], (HAS_Z ? 3u : 2u) * Wt::SEQ + (CK ? 1u : 2u) * Wt::BC);
+            mbar_arrive_expect_tx(&tma_full[s], (HAS_Z ? 3u : 2u) * Wt::SEQ + (OUTY ? 2u : 1u) * Wt::BC);
 #pragma unroll
             for (int j = 0; j < NB8; ++j) {
                 tma_load_3d(st + Wt::off_u + j * Wt::BLK, &maps.u, &tma_full[s], t0 + 8 * j, it.d0, it.b);
@@ -716,7 +720,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 if (HAS_Z) tma_load_3d(st + Wt::off_z + j * Wt::BLK, &maps.z, &tma_full[s], t0 + 8 * j, it.d0, it.b);
             }
             tma_load_3d(st + Wt::off_B, &maps.B, &tma_full[s], 0, t0, it.b);
-            if (!CK) tma_load_3d(st + Wt::off_C, &maps.C, &tma_full[s], 0, t0, it.b);
+            if (OUTY) tma_load_3d(st + Wt::off_C, &maps.C, &tma_full[s], 0, t0, it.b);
         };
         bool ok = true;
         // Publishes the end of the work in slot 0 after `tiles` tiles went out.
@@ -781,7 +785,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     const float2 uu = make_float2(uf[2 * j], uf[2 * j + 1]);
                     const float2 du = mul2(x, uu);
                     dd[j] = make_float4(x.x, x.y, du.x, du.y);
-                    if (!CK) {
+                    if (OUTY) {
                         const float2 gt = HAS_Z ? gate2<T>(make_float2(zf[2 * j], zf[2 * j + 1])) : make_float2(1.f, 1.f);
                         const float2 dg = mul2(mul2(make_float2(skip, skip), uu), gt);
                         gd[j] = make_float4(gt.x, gt.y, dg.x, dg.y);
@@ -829,6 +833,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     int d = 0;
     bool live = false;
     int ostage = 0;
+    float dsum = 0.f;  // Σ Δ over the item (aggregate pass)
     bool failed = false;
     for (uint32_t i = 0;; ++i) {
         const int s = i & 1;
@@ -855,9 +860,12 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 A2[q] = make_float2(av[0], av[1]);
                 h[q] = make_float2(0.f, 0.f);
             }
+            dsum = 0.f;
             const float *src = nullptr;
             bool cg = false;  // read through L2 only: another SM wrote it during this launch
-            if (it.k == 0) {
+            if (AG) {
+                // every aggregate starts from a zero state
+            } else if (it.k == 0) {
                 src = a.h0 ? a.h0 + ((size_t)it.b * D + d) * N : nullptr;
             } else if (chained) {
                 if (lane == 0 && !wait_flag(a.flags + it.grp, it.k, kFlagLimit))
@@ -886,7 +894,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             break;
         }
         // The y tile written two tiles ago must have left shared memory.
-        if (!CK && lane == 0) bulk_wait_read1();
+        if (OUTY && lane == 0) bulk_wait_read1();
         __syncwarp();
         const int t0 = it.t_begin + tile * kTT;
         const unsigned char *st = stage(s);
@@ -984,14 +992,15 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     }
 #pragma unroll
                     for (int q = 0; q < NQ; ++q) h[q] = fma2(ac[q], h[q], bc[q]);
-                    if (!CK) {
+                    if (AG) dsum += (j & 1) ? dl[j >> 1].y : dl[j >> 1].x;
+                    if (OUTY) {
                         if (j > 0) readout(j - 1, hp, Cnx);
                         load_row(Cf, j, Cnx);
 #pragma unroll
                         for (int q = 0; q < NQ; ++q) hp[q] = h[q];
                     }
                 }
-                if (CK) continue;
+                if (!OUTY) continue;
                 readout(7, hp, Cnx);
                 // Transposed sum over the two lanes of a channel: lane g keeps
                 // tokens 4g .. 4g+3, whose gate terms sit in pairs 2g, 2g+1.
@@ -1011,7 +1020,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             ws_arrive(&trm_empty[hh]);  // this half's terms are read
         }
         if (failed) break;
-        if (!CK) {
+        if (OUTY) {
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -1023,7 +1032,21 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
         }
         __syncwarp();
         ws_arrive(&stage_empty[s]);  // this tile's B, C rows are read
-        if (hd.z & kWsLast) {
+        if (AG && (hd.z & kWsLast) && live) {
+            // ---- item end (aggregate pass): the chunk's (Π Ā, h_end from zero)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int n = SPT * g + 2 * q + j;
+                    const float av = j ? A2[q].y : A2[q].x;
+                    const float hv = j ? h[q].y : h[q].x;
+                    if (n < N)
+                        a.agg[(((size_t)it.b * D + d) * (K - 1) + it.k) * N + n] = make_float2(ex2(av * dsum), hv);
+                }
+            }
+        }
+        if (!AG && (hd.z & kWsLast)) {
             // ---- item end: hand the state on, or write the final state
             float *dst = nullptr;
             const bool last = it.k == K - 1;
@@ -1046,7 +1069,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
         }
     }
     if (failed) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
-    if (!CK && lane == 0) bulk_wait0();
+    if (OUTY && lane == 0) bulk_wait0();
 }
 
 // B and C, [b][N][L] in the I/O type, widened once per launch to fp32
@@ -1173,10 +1196,10 @@ cudaError_t launch_one(const Maps &maps, const ScanArgs &a, int items, cudaStrea
     return cudaGetLastError();
 }
 
-template <typename T, bool HAS_Z, bool ZOH, bool CK = false>
+template <typename T, bool HAS_Z, bool ZOH, int WM = 0>
 cudaError_t launch_ws(const Maps &maps, const ScanArgs &a, int items, cudaStream_t st) {
     using S = WsTile<T>;
-    auto kern = scan_ws_kernel<T, HAS_Z, ZOH, CK>;
+    auto kern = scan_ws_kernel<T, HAS_Z, ZOH, WM>;
     static int per_sm = 0;  // resident CTAs (four consumer warps each) per SM
     if (per_sm == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::bytes);
@@ -1200,18 +1223,19 @@ cudaError_t launch_all(const Maps &maps, const ScanArgs &a, cudaStream_t st) {
     widen_bc_kernel<T><<<dim3((a.seqlen + 31) / 32, a.batch), 256, 0, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // bf16 I/O, first order: the warp-specialised form keeps eight consumer
+    // warps per SM within 128 registers and 26 KB of shared memory per CTA.
+    constexpr bool ws = SSM_SCAN_WS && TMA && SPT == 8 && NG == 2 && sizeof(T) == 2 && !ZOH;
     if (a.nchunks > 1 && !a.chained) {
-        e = launch_one<T, SPT, NG, false, TMA, 1, ZOH>(maps, a, a.groups * (a.nchunks - 1), st);
+        if constexpr (ws) e = launch_ws<T, false, ZOH, 1>(maps, a, a.groups * (a.nchunks - 1), st);
+        else e = launch_one<T, SPT, NG, false, TMA, 1, ZOH>(maps, a, a.groups * (a.nchunks - 1), st);
         if (e != cudaSuccess) return e;
         const size_t total = (size_t)a.batch * a.dim * a.dstate;
         carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    // bf16 I/O, first order: the warp-specialised form keeps eight consumer
-    // warps per SM within 128 registers and 26 KB of shared memory per CTA.
-    if constexpr (SSM_SCAN_WS && TMA && SPT == 8 && NG == 2 && sizeof(T) == 2 && !ZOH)
-        return launch_ws<T, HAS_Z, ZOH>(maps, a, a.groups * a.nchunks, st);
+    if constexpr (ws) return launch_ws<T, HAS_Z, ZOH>(maps, a, a.groups * a.nchunks, st);
     return launch_one<T, SPT, NG, HAS_Z, TMA, 0, ZOH>(maps, a, a.groups * a.nchunks, st);
 }
 
@@ -1309,7 +1333,7 @@ cudaError_t scan_ckpt_launch(const ScanArgs &a, cudaStream_t st) {
     widen_bc_kernel<T><<<dim3((a.seqlen + 31) / 32, a.batch), 256, 0, st>>>(a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_ws<T, false, false, true>(maps, a, a.groups * a.nchunks, st);
+    return launch_ws<T, false, false, 2>(maps, a, a.groups * a.nchunks, st);
 }
 
 cudaError_t scan_launch(const ScanArgs &a, bool bf16, cudaStream_t st) {
