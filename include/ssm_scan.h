@@ -99,7 +99,7 @@ size_t ssm_scan_workspace_size(const ssm_scan_params *p);
  * chunks K, out[2] = 1 if chunk k starts from the state chunk k-1 hands over
  * (one scan launch) or 0 if an aggregate pass and a carry pass precompute the
  * chunks' starting states (three launches when K > 1), out[3] = number of
- * channel groups (one warp each).  Every scan is preceded by one small launch
+ * channel groups (one scanning warp each).  Every scan is preceded by one small launch
  * that widens B and C to fp32 token-major rows in the workspace.  Returns SSM_ERR_INVALID_ARG for invalid
  * sizes or a NULL out. */
 ssm_status ssm_scan_plan(const ssm_scan_params *p, int64_t out[4]);

@@ -604,9 +604,9 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     if (TMA && MODE == 0 && lane == 0) bulk_wait0();
 }
 
-// ------------------------------------------------------- warp-specialised main pass
-// The main pass (MODE 0) with TMA and two lanes per channel, as producer /
-// consumer warp pairs.  The producer takes the work items, issues each tile's
+// ------------------------------------------------------- warp-specialised passes
+// The passes with TMA and two lanes per channel (bf16 I/O, first order), as
+// producer / consumer warp pairs.  The producer takes the work items, issues each tile's
 // loads and forms every token's terms — Δ = softplus(Δraw + bias), Δ·u, the
 // gate and D·u·gate — into shared memory, half a tile (16 tokens) at a time;
 // the consumer runs the recurrence and the read-out of the same tile from those
