@@ -292,8 +292,18 @@ def test_bwd_workspace_size_with_forward_checkpoints():
     base = 256 + 2 * flags + 2 * bdn + groups * ntiles * 1024
     p = valid_bwd(batch=b, dim=d, seqlen=L)
     assert capi.ssm_scan_bwd_workspace_size(p) == base + flags + bdn + 2 * bt
-    # the zero-order hold keeps the backward's own checkpoint pass
+    # the zero-order hold keeps the backward's own checkpoint pass, as do fp32
+    # I/O, too few channel groups for a chained forward plan, and a row pitch
+    # TMA cannot describe
     assert capi.ssm_scan_bwd_workspace_size(valid_bwd(batch=b, dim=d, seqlen=L, zoh=1)) == base
+    assert capi.ssm_scan_bwd_workspace_size(valid_bwd(batch=b, dim=d, seqlen=L, io_dtype=capi.SSM_F32)) == base
+    small = valid_bwd(batch=1, dim=d, seqlen=L)                # 320 groups: a two-pass forward plan
+    g1 = d // 16
+    assert capi.ssm_scan_bwd_workspace_size(small) == (
+        256 + 2 * (-(-g1 * 4 // 256) * 256) + 2 * (-(-d * n * 4 // 256) * 256) + g1 * ntiles * 1024)
+    odd = valid_bwd(batch=b, dim=d, seqlen=L - 1)              # 2·L bytes not a multiple of 16
+    assert capi.ssm_scan_bwd_workspace_size(odd) == (
+        256 + 2 * flags + 2 * bdn + groups * -(-(L - 1) // 16) * 1024)
 
 
 def valid_ssd(**over):
