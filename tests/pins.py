@@ -549,8 +549,46 @@ def pin_mamba2_counts(lib):
     assert layer == g["m2_layer_weights"]
 
 
+# P16: for fixed Δraw, B, C and z the selective scan is a linear time-varying
+# system in its input and its initial state (erikxu.me notes — "State Space
+# Models": h_t = Ā_t h_{t−1} + B̄_t x_t, y_t = C_t h_t; datarekha.com — "One
+# system, two views": the D·x skip; the gate multiplies each token's output by
+# silu(z_t), a fixed scale here): superposition holds for y and h_L, in both
+# discretisations and in the decode step.
+
+def pin_superposition(lib, seed=24):
+    rng = np.random.default_rng(seed)
+    b, dim, N, L = 2, 3, 5, 17
+    A = -rng.uniform(0.1, 2.0, (dim, N))
+    dr = rng.normal(size=(b, dim, L))
+    z = rng.normal(size=(b, dim, L))
+    B = rng.normal(size=(b, N, L))
+    C = rng.normal(size=(b, N, L))
+    Dsk = rng.normal(size=dim)
+    bias = rng.normal(size=dim)
+    u1, u2 = rng.normal(size=(b, dim, L)), rng.normal(size=(b, dim, L))
+    h1, h2 = rng.normal(size=(b, dim, N)), rng.normal(size=(b, dim, N))
+    al, be = 0.7, -1.3
+    for zoh in (False, True):
+        kw = dict(Dskip=Dsk, z=z, bias=bias, zoh=zoh, lib=lib)
+        y1, s1 = orc.scan(u1, dr, A, B, C, h0=h1, **kw)
+        y2, s2 = orc.scan(u2, dr, A, B, C, h0=h2, **kw)
+        y, st = orc.scan(al * u1 + be * u2, dr, A, B, C, h0=al * h1 + be * h2, **kw)
+        _close(y, al * y1 + be * y2, 1e-12, 1e-13, f"superposition y (zoh={zoh})")
+        _close(st, al * s1 + be * s2, 1e-12, 1e-13, f"superposition h_L (zoh={zoh})")
+        t = 5
+        ya, sa = orc.step(h1.copy(), u1[..., t], dr[..., t], A, B[..., t], C[..., t], Dskip=Dsk,
+                          z=z[..., t], bias=bias, zoh=zoh, lib=lib)
+        yb, sb = orc.step(h2.copy(), u2[..., t], dr[..., t], A, B[..., t], C[..., t], Dskip=Dsk,
+                          z=z[..., t], bias=bias, zoh=zoh, lib=lib)
+        yc, sc = orc.step(al * h1 + be * h2, al * u1[..., t] + be * u2[..., t], dr[..., t], A, B[..., t],
+                          C[..., t], Dskip=Dsk, z=z[..., t], bias=bias, zoh=zoh, lib=lib)
+        _close(yc, al * ya + be * yb, 1e-12, 1e-13, f"superposition decode y (zoh={zoh})")
+        _close(sc, al * sa + be * sb, 1e-12, 1e-13, f"superposition decode state (zoh={zoh})")
+
+
 ALL_PINS = [pin_worked_example, pin_lti_convolution, pin_gated_rnn, pin_delta_limits,
             pin_first_output, pin_product_form, pin_continuation, pin_decode_equals_scan,
             pin_conv_library, pin_conv_impulse, pin_conv_continuation, pin_block_counts,
             pin_backward_finite_differences, pin_ssd_is_mamba1_with_scalar_A, pin_ssd_matrix_form,
-            pin_mamba2_counts]
+            pin_mamba2_counts, pin_superposition]
