@@ -71,6 +71,10 @@ MUTANTS = {
     "ssd_dt_bias_dropped": ("double d = dt[(b * L + t) * H + h] + (dt_bias ? dt_bias[h] : 0.0);",
                             "double d = dt[(b * L + t) * H + h];"),
     "ssd_A_of_head_0": ("const double a = exp(d * A[h]);", "const double a = exp(d * A[0]);"),
+    # mistakes that break linearity in the input (caught by superposition, P16)
+    "state_update_constant_term": ("h[n] = abar * h[n] + bbar * u_c[t];",
+                                   "h[n] = abar * h[n] + bbar * u_c[t] + 1e-3 * dt;"),
+    "skip_term_squared": ("double out = s + skip * u_c[t];", "double out = s + skip * u_c[t] * fabs(u_c[t]);"),
 }
 
 
