@@ -320,7 +320,12 @@ ssm_status ssm_conv1d_step(const ssm_conv_step_params *p, ssm_stream_t stream);
  * frees nothing.
  *   - The first call on a device looks up the array's device address with
  *     cudaGetSymbolAddress (with that device current) and caches it; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  cudaDeviceReset destroys the
+ *     array with the context and the cached address then points at freed
+ *     memory: a process that resets a device must not call this entry point
+ *     on that device again.
+ *   - The library's kernels and this array are set up per device, so a
+ *     process may call it on several devices, each with its own array.
  *   - Sizes whose scratch need (ssm_scan_workspace_size) exceeds
  *     SSM_NOALLOC_SCRATCH_BYTES are rejected with SSM_ERR_UNSUPPORTED before
  *     anything is launched; other argument errors are those of ssm_scan_fwd.

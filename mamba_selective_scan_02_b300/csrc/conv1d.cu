@@ -428,19 +428,19 @@ cudaError_t launch_seq(const ConvArgs &a, cudaStream_t stream) {
                      (reinterpret_cast<uintptr_t>(a.u) % 16) == 0 && es * 8 % 16 == 0 && units < (INT32_MAX / 2);
     if (vec) {
         // persistent: as many blocks as fit at once
-        static int resident = 0;  // blocks per SM, per instantiation
-        if (resident == 0) {
-            int per_sm = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, conv1d_stream_kernel<T, W, SILU>,
-                                                              kConvThreads, 0) != cudaSuccess)
-                return cudaGetLastError();
-            resident = per_sm > 0 ? per_sm : 1;
-        }
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return cudaGetLastError();
-        const int64_t grid = std::min<int64_t>(blocks, (int64_t)resident * sms);
+        static PerDevice per_device;  // blocks per SM, per instantiation
+        int resident = 0;
+        const cudaError_t e = per_device.get(
+            [&](int *v) {
+                int per_sm = 0;
+                const cudaError_t r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    &per_sm, conv1d_stream_kernel<T, W, SILU>, kConvThreads, 0);
+                *v = per_sm > 0 ? per_sm : 1;
+                return r;
+            },
+            &resident);
+        if (e != cudaSuccess) return e;
+        const int64_t grid = std::min<int64_t>(blocks, (int64_t)resident * sm_count());
         conv1d_stream_kernel<T, W, SILU><<<(unsigned)grid, kConvThreads, 0, stream>>>(a);
     } else {
         conv1d_kernel<T, W, SILU, false><<<(unsigned)blocks, kConvThreads, 0, stream>>>(a);

@@ -639,9 +639,15 @@ cudaError_t launch_pair(const BwdArgs &a, cudaStream_t st) {
     cudaError_t e = cudaSuccess;
     if (!a.ckpt_ready) {
         auto k1 = bwd_ckpt_kernel<T, NG, ZOH, VEC>;
-        static int res1 = 0;
-        if (res1 == 0) res1 = resident_warps(reinterpret_cast<const void *>(k1), 0);
-        if (res1 == 0) return cudaErrorInvalidConfiguration;
+        static PerDevice per_device1;
+        int res1 = 0;
+        e = per_device1.get(
+            [&](int *v) {
+                *v = resident_warps(reinterpret_cast<const void *>(k1), 0);
+                return *v > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+            },
+            &res1);
+        if (e != cudaSuccess) return e;
         k1<<<std::max(1, std::min(items, res1)), 32, 0, st>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -649,13 +655,17 @@ cudaError_t launch_pair(const BwdArgs &a, cudaStream_t st) {
 
     auto k2 = bwd_rev_kernel<T, NG, HAS_Z, ZOH, VEC>;
     constexpr size_t smem = sizeof(RevSmem<NG>);
-    static int res2 = 0;
-    if (res2 == 0) {
-        e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        res2 = resident_warps(reinterpret_cast<const void *>(k2), smem);
-    }
-    if (res2 == 0) return cudaErrorInvalidConfiguration;
+    static PerDevice per_device2;
+    int res2 = 0;
+    e = per_device2.get(
+        [&](int *v) {
+            const cudaError_t r = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (r != cudaSuccess) return r;
+            *v = resident_warps(reinterpret_cast<const void *>(k2), smem);
+            return *v > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+        },
+        &res2);
+    if (e != cudaSuccess) return e;
     k2<<<std::max(1, std::min(items, res2)), 32, smem, st>>>(a);
     return cudaGetLastError();
 }

@@ -1179,19 +1179,20 @@ template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, int MODE, bool ZOH>
 cudaError_t launch_one(const Maps &maps, const ScanArgs &a, int items, cudaStream_t st) {
     using S = WTile<T, SPT, NG>;
     auto kern = scan_kernel<T, SPT, NG, HAS_Z, TMA, MODE, ZOH>;
-    static int per_sm = 0;  // resident warps per SM for this instantiation
-    if (per_sm == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::bytes);
-        if (e != cudaSuccess) return e;
-        int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32, S::bytes);
-        if (e != cudaSuccess) return e;
-        per_sm = std::max(1, std::min(n, kWarpsPerSM));
-    }
-    int sms = kSMs;
-    int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = std::max(1, std::min(items, sms * per_sm));
+    static PerDevice resident;  // resident warps per SM for this instantiation
+    int per_sm = 0;
+    cudaError_t e = resident.get(
+        [&](int *v) {
+            cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::bytes);
+            if (r != cudaSuccess) return r;
+            int n = 0;
+            r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32, S::bytes);
+            *v = std::max(1, std::min(n, kWarpsPerSM));
+            return r;
+        },
+        &per_sm);
+    if (e != cudaSuccess) return e;
+    const int grid = std::max(1, std::min(items, sm_count() * per_sm));
     kern<<<grid, 32, S::bytes, st>>>(maps, a);
     return cudaGetLastError();
 }
@@ -1200,19 +1201,20 @@ template <typename T, bool HAS_Z, bool ZOH, int WM = 0>
 cudaError_t launch_ws(const Maps &maps, const ScanArgs &a, int items, cudaStream_t st) {
     using S = WsTile<T>;
     auto kern = scan_ws_kernel<T, HAS_Z, ZOH, WM>;
-    static int per_sm = 0;  // resident CTAs (four consumer warps each) per SM
-    if (per_sm == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::bytes);
-        if (e != cudaSuccess) return e;
-        int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * 2 * S::PAIRS, S::bytes);
-        if (e != cudaSuccess) return e;
-        per_sm = std::max(1, std::min(n, kWarpsPerSM / S::PAIRS));
-    }
-    int sms = kSMs;
-    int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int pairs = std::max(1, std::min(items, sms * per_sm * S::PAIRS));
+    static PerDevice resident;  // resident CTAs (four consumer warps each) per SM
+    int per_sm = 0;
+    cudaError_t e = resident.get(
+        [&](int *v) {
+            cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::bytes);
+            if (r != cudaSuccess) return r;
+            int n = 0;
+            r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * 2 * S::PAIRS, S::bytes);
+            *v = std::max(1, std::min(n, kWarpsPerSM / S::PAIRS));
+            return r;
+        },
+        &per_sm);
+    if (e != cudaSuccess) return e;
+    const int pairs = std::max(1, std::min(items, sm_count() * per_sm * S::PAIRS));
     kern<<<(pairs + S::PAIRS - 1) / S::PAIRS, 32 * 2 * S::PAIRS, S::bytes, st>>>(maps, a);
     return cudaGetLastError();
 }

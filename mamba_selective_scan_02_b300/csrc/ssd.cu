@@ -402,12 +402,15 @@ bool ssd_supported(int64_t headdim, int64_t dstate) { return headdim == P && dst
 
 cudaError_t ssd_launch(const SsdArgs &a, cudaStream_t st) {
     constexpr size_t smem = sizeof(SsdSmem);
-    static bool attr = false;
-    if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(ssd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static PerDevice attr;  // the shared-memory limit is raised once per device
+    int done = 0;
+    const cudaError_t e = attr.get(
+        [&](int *v) {
+            *v = 1;
+            return cudaFuncSetAttribute(ssd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        },
+        &done);
+    if (e != cudaSuccess) return e;
     ssd_kernel<<<a.batch * a.nheads, kThreads, smem, st>>>(a);
     return cudaGetLastError();
 }

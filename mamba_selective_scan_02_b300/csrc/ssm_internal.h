@@ -4,7 +4,50 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace ssm {
+
+// One launch-configuration value per device (a kernel's raised dynamic
+// shared-memory limit and its occupancy are properties of the kernel on one
+// device).  Each launch site keeps one of these as a function-local static;
+// the first launch on a device computes that device's value under the lock,
+// setting whatever kernel attributes it needs on the way.
+class PerDevice {
+  public:
+    template <typename Fill>
+    cudaError_t get(Fill fill, int *out) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> hold(lock_);
+        if (!ready_[dev]) {
+            int v = 0;
+            e = fill(&v);
+            if (e != cudaSuccess) return e;
+            value_[dev] = v;
+            ready_[dev] = true;
+        }
+        *out = value_[dev];
+        return cudaSuccess;
+    }
+
+  private:
+    static constexpr int kMaxDevices = 64;
+    std::mutex lock_;
+    int value_[kMaxDevices] = {};
+    bool ready_[kMaxDevices] = {};
+};
+
+// Streaming multiprocessors of the current device (148 on a B300).
+inline int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return 148;
+    return sms;
+}
 
 // Validated, device-side view of one forward scan (sizes fit in int32).
 struct ScanArgs {

@@ -345,22 +345,25 @@ cudaError_t stream_dispatch(const StepArgs &a, cudaStream_t st) {
     using S = StreamTile<T>;
     const int smem = kStreamStages * S::bytes + 64;
     const int ntiles = (int)((size_t)a.batch * a.dim / kStreamCh);
-    static int grid_cap = 0;
-    if (grid_cap == 0) {
-        auto k0 = step_stream_kernel<T, false, false>;
-        auto k1 = step_stream_kernel<T, true, false>;
-        auto k2 = step_stream_kernel<T, false, true>;
-        auto k3 = step_stream_kernel<T, true, true>;
-        if (cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-            cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-            cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-            cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return cudaGetLastError();
-        int per_sm = 0, dev = 0, sms = 148;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k1, kStreamCh, smem) != cudaSuccess) return cudaGetLastError();
-        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        grid_cap = sms * (per_sm > 0 ? per_sm : 1);
-    }
+    static PerDevice per_device;
+    int grid_cap = 0;
+    const cudaError_t e = per_device.get(
+        [&](int *v) {
+            auto k0 = step_stream_kernel<T, false, false>;
+            auto k1 = step_stream_kernel<T, true, false>;
+            auto k2 = step_stream_kernel<T, false, true>;
+            auto k3 = step_stream_kernel<T, true, true>;
+            cudaError_t r = cudaSuccess;
+            for (auto k : {k0, k1, k2, k3})
+                if (r == cudaSuccess) r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (r != cudaSuccess) return r;
+            int per_sm = 0;
+            r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k1, kStreamCh, smem);
+            *v = sm_count() * (per_sm > 0 ? per_sm : 1);
+            return r;
+        },
+        &grid_cap);
+    if (e != cudaSuccess) return e;
     const int grid = ntiles < grid_cap ? ntiles : grid_cap;
     if (a.zoh) {
         if (a.z) step_stream_kernel<T, true, true><<<grid, kStreamCh, smem, st>>>(a);
