@@ -73,10 +73,15 @@ def scan_params(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None, *, 
     return p
 
 
-def workspace_bytes(u, delta, A, B, C, chunk_len=0) -> int:
+def workspace_bytes(u, delta, A, B, C, chunk_len=0, zoh=False) -> int:
+    """Workspace bytes for a scan of these tensors: the plan, and with it the
+    workspace, depends on the sizes, the I/O dtype, the discretisation and
+    chunk_len."""
     p = capi.ScanParams()
     p.batch, p.dim, p.seqlen = u.shape
     p.dstate = A.shape[1]
+    p.io_dtype = capi.SSM_BF16 if u.dtype == torch.bfloat16 else capi.SSM_F32
+    p.zoh = 1 if zoh else 0
     p.chunk_len = int(chunk_len)
     n = capi.ssm_scan_workspace_size(p)
     if n == 0:
@@ -93,7 +98,7 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None, *,
     if hL is None and return_last_state:
         hL = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
     if workspace is None:
-        workspace = torch.empty(workspace_bytes(u, delta, A, B, C, chunk_len), dtype=torch.uint8,
+        workspace = torch.empty(workspace_bytes(u, delta, A, B, C, chunk_len, zoh), dtype=torch.uint8,
                                 device=u.device)
     p = scan_params(u, delta, A, B, C, D, z, delta_bias, h0, y=y, hL=hL,
                     delta_softplus=delta_softplus, zoh=zoh, chunk_len=chunk_len, workspace=workspace)
