@@ -231,9 +231,14 @@ typedef struct {
     const float *h0;                 /* b × H × P × N fp32; NULL = zeros */
     void *y;                         /* out: b × L × H × P */
     float *hL;                       /* out: b × H × P × N fp32; NULL = not written */
+    int32_t *status;                 /* device int or NULL: a bounded wait inside the kernel
+                                        that ran out stores SSM_ERR_TIMEOUT here if it still
+                                        holds 0 (the caller zeroes it and reads it back) */
 } ssm_ssd_params;
 
-/* The Mamba-2 layer scan; one launch, no workspace. */
+/* The Mamba-2 layer scan; one launch, no workspace.  The kernel's waits on
+ * its own copies and products are bounded; when one runs out, y and hL are
+ * incomplete and the status word (if given) says SSM_ERR_TIMEOUT. */
 ssm_status ssm_ssd_fwd(const ssm_ssd_params *p, ssm_stream_t stream);
 
 /* ------------------------------------------------------------------------

@@ -68,7 +68,7 @@ class SsdParams(ctypes.Structure):
         ("io_dtype", ctypes.c_int),
         ("x", _vp), ("dt", _vp), ("A", _vp), ("B", _vp), ("C", _vp),
         ("Dskip", _vp), ("dt_bias", _vp), ("dt_softplus", ctypes.c_int),
-        ("h0", _vp), ("y", _vp), ("hL", _vp),
+        ("h0", _vp), ("y", _vp), ("hL", _vp), ("status", _vp),
     ]
 
 

@@ -390,7 +390,7 @@ ssm_status ssm_ssd_fwd(const ssm_ssd_params *p, ssm_stream_t stream) {
     for (const void *q : a16)
         if (!aligned16(q)) return SSM_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(p->dt) % 2 != 0) return SSM_ERR_INVALID_ARG;
-    const void *a4[] = {p->A, p->Dskip, p->dt_bias, p->h0, p->hL};
+    const void *a4[] = {p->A, p->Dskip, p->dt_bias, p->h0, p->hL, p->status};
     for (const void *q : a4)
         if (q && !aligned4(q)) return SSM_ERR_INVALID_ARG;
     const size_t seq = (size_t)p->batch * p->seqlen * p->nheads * p->headdim * 2;
@@ -413,6 +413,7 @@ ssm_status ssm_ssd_fwd(const ssm_ssd_params *p, ssm_stream_t stream) {
     a.h0 = p->h0;
     a.y = p->y;
     a.hL = p->hL;
+    a.status = p->status;
     return ssm::ssd_launch(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

@@ -1130,26 +1130,24 @@ __global__ void carry_kernel(const ScanArgs a) {
 
 // ------------------------------------------------------------------ host side
 
-namespace {
-
-using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn encode_fn() {
-    static EncodeFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+TensorMapEncodeFn tensor_map_encoder() {
+    static TensorMapEncodeFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeFn>(p);
-    }
+            fn = reinterpret_cast<TensorMapEncodeFn>(p);
+    });
     return fn;
 }
+
+namespace {
+
+using EncodeFn = TensorMapEncodeFn;
+EncodeFn encode_fn() { return tensor_map_encoder(); }
 
 // 3-D map over a (dim2 × dim1 × dim0) row-major tensor, box (box0, box1, 1).
 bool make_map(CUtensorMap *m, CUtensorMapDataType dt, size_t es, const void *ptr, uint64_t dim0, uint64_t dim1,

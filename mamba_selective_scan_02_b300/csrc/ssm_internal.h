@@ -1,6 +1,7 @@
 // ssm_internal.h — argument structs shared by the C-ABI layer and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -39,6 +40,14 @@ class PerDevice {
     int value_[kMaxDevices] = {};
     bool ready_[kMaxDevices] = {};
 };
+
+// cuTensorMapEncodeTiled, fetched from the driver once per process (thread
+// safe); null when the driver does not provide it.
+using TensorMapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                       const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                       CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                       CUtensorMapFloatOOBfill);
+TensorMapEncodeFn tensor_map_encoder();
 
 // Streaming multiprocessors of the current device (148 on a B300).
 inline int sm_count() {
@@ -128,6 +137,7 @@ struct SsdArgs {
     const float *h0;                 // b × H × P × N fp32 or null
     void *y;                         // b × L × H × P
     float *hL;                       // b × H × P × N fp32 or null
+    int *status;                     // device status word or null
 };
 
 // Causal depthwise convolution + bias + optional SiLU over whole sequences.

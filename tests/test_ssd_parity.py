@@ -2,9 +2,9 @@
 
 The kernel multiplies bf16 operands on the tensor cores with fp32
 accumulation: x, B, C enter as the bf16 inputs themselves, while the decay-
-masked C·Bᵀ block, the B scaled by the state weights and the carried state are
-rounded to bf16 as operands (half a bf16 ulp, 2^-9 relative, each) before
-sums of 64 to 128 terms.  The contract's bf16 tolerance, |err| <=
+masked C·Bᵀ block, the x scaled by the state weights and the carried state
+enter as a bf16 value plus a bf16 remainder (about 2^-17 relative each)
+before sums of 128 terms.  The contract's bf16 tolerance, |err| <=
 2e-2·(1 + |y|), covers it; the final state (fp32, built from such products) is
 held to the same bound relative to its scale.
 """
@@ -46,10 +46,11 @@ def run(inp, softplus=True):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("shape", [(2, 200, 3),    # ragged: three full chunks and a partial one
-                                   (1, 64, 2),     # exactly one chunk
+@pytest.mark.parametrize("shape", [(2, 300, 3),    # ragged: two full 128-token chunks and a partial one
+                                   (1, 128, 2),    # exactly one chunk
                                    (1, 1, 1),      # a single token
-                                   (3, 130, 5)])
+                                   (3, 130, 5),    # one chunk and two tokens
+                                   (1, 520, 2)])   # four chunks and a short tail
 @pytest.mark.parametrize("h0", [False, True])
 def test_ssd_every_element(shape, h0):
     b, L, H = shape
@@ -86,3 +87,32 @@ def test_ssd_mamba2_layer_sampled():
                          Dskip=inp["D"][h:h + 1].cpu(), dt_bias=inp["dt_bias"][h:h + 1].cpu())
         check(f"y[{bi}, :, {h}]", y[bi:bi + 1, :, h:h + 1], wy)
         check(f"hL[{bi}, {h}]", hL[bi:bi + 1, h:h + 1], wh, scale=1.0 + np.abs(wh) + np.sqrt(np.mean(wh ** 2)))
+
+
+def _poisoned(shape, dtype, pad=4096):
+    """A tensor of `shape` at the front of a larger buffer whose tail holds a
+    fixed bit pattern, so that a write past the end shows."""
+    n = int(np.prod(shape))
+    buf = torch.empty(n + pad, dtype=dtype, device="cuda")
+    buf.view(torch.int16 if dtype == torch.bfloat16 else torch.int32).fill_(0x7B3D)
+    return buf[:n].view(shape), buf[n:], buf[n:].clone()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("L", [1, 127, 129, 300])
+def test_ssd_writes_nothing_past_y_and_hL(L):
+    b, H, P, N = 2, 3, 64, 128
+    inp = make_ssd_inputs(b, L, H, seed=11 + L, device="cuda", with_h0=True)
+    y, ytail, yref = _poisoned((b, L, H, P), torch.bfloat16)
+    hL, htail, href = _poisoned((b, H, P, N), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["dt_bias"], inp["h0"],
+                y=y, hL=hL, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(ytail, yref), "y: bytes past the end were written"
+    assert torch.equal(htail, href), "hL: bytes past the end were written"
+    c = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    wy, wh = orc.ssd(c["x"], c["dt"], c["A"], c["B"], c["C"], Dskip=c["D"], dt_bias=c["dt_bias"], h0=c["h0"])
+    check("y", y, wy)
+    check("hL", hL, wh, scale=1.0 + np.abs(wh) + np.sqrt(np.mean(wh ** 2)))
