@@ -55,7 +55,8 @@ typedef enum {
     SSM_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, small workspace */
     SSM_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement (e.g. dstate > 16) */
     SSM_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
-    SSM_ERR_TIMEOUT = 4      /* a device-side bounded wait ran out (reported via the workspace) */
+    SSM_ERR_TIMEOUT = 4,     /* a device-side bounded wait ran out (reported via the workspace) */
+    SSM_ERR_BOUNDS = 5       /* debug build only: an index check found a store outside its buffer */
 } ssm_status;
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
@@ -348,6 +349,14 @@ ssm_status ssm_workspace_status(const void *workspace, ssm_stream_t stream);
 
 /* Static description of a status code. */
 const char *ssm_status_string(ssm_status s);
+
+/* Debug build (compiled with -DSSM_DEBUG, libssmscan_debug.so): every kernel
+ * checks the element range of each global store against the buffer it writes,
+ * skips a store that falls outside and records SSM_ERR_BOUNDS in a device word
+ * of its source file; no check traps.  Synchronises the device, then returns
+ * SSM_OK or SSM_ERR_BOUNDS (SSM_ERR_CUDA if a word cannot be read); `reset`
+ * non-zero clears the words.  The release build returns SSM_ERR_UNSUPPORTED. */
+ssm_status ssm_debug_status(int reset);
 
 /* Measurement helper (not part of the method): launches `blocks` × 256 threads
  * that each evaluate 16 × iters dependent-free ex2.approx.ftz.f32 chains and

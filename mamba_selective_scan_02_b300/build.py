@@ -16,6 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libssmscan.so")
+LIB_DEBUG = os.path.join(LIBDIR, "libssmscan_debug.so")   # -DSSM_DEBUG: index checks on every store
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,17 +45,21 @@ def nvcc_cmd(out: str, extra=()):
             + sources())
 
 
-def build(force: bool = False, verbose: bool = False, extra=(), jobs: int = 0) -> str:
+def build(force: bool = False, verbose: bool = False, extra=(), jobs: int = 0, debug: bool = False) -> str:
     """Compile the library if any source is newer than it.  Returns its path.
 
     Each source compiles to its own object in a separate nvcc process (the
     files share no device code, only inline header functions), in parallel,
-    and one nvcc call links them."""
-    if not force and not stale():
-        return LIB
+    and one nvcc call links them.  `debug` builds libssmscan_debug.so with
+    -DSSM_DEBUG instead."""
+    out = LIB_DEBUG if debug else LIB
+    if debug:
+        extra = (*extra, "-DSSM_DEBUG")
+    if not force and not stale(out):
+        return out
     from concurrent.futures import ThreadPoolExecutor
     os.makedirs(LIBDIR, exist_ok=True)
-    tag = "%d" % os.getpid()
+    tag = "%d%s" % (os.getpid(), "d" if debug else "")
     objdir = os.path.join(LIBDIR, "obj." + tag)
     os.makedirs(objdir, exist_ok=True)
     inc = ["-I", os.path.join(ROOT, "include")]
@@ -73,16 +78,15 @@ def build(force: bool = False, verbose: bool = False, extra=(), jobs: int = 0) -
             raise subprocess.CalledProcessError(r.returncode, c)
         if verbose and (r.stdout or r.stderr):
             sys.stderr.write(r.stdout + r.stderr)
-    tmp = LIB + ".tmp" + tag
+    tmp = out + ".tmp" + tag
     subprocess.run(["nvcc", *ARCH, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
+    os.replace(tmp, out)
     for o in objs:
         os.remove(o)
     os.rmdir(objdir)
-    return LIB
+    return out
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True,
-          extra=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else ())
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv,
+                extra=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else ()))

@@ -3,6 +3,8 @@
 Structs and prototypes mirror the header one to one.  The library is opened on
 first use from this package's ``lib/`` directory; if it is missing it is built
 in-tree with nvcc, and if that fails the call raises — there is no fallback.
+With the environment variable SSM_SCAN_LIBRARY=debug the process opens the
+debug build instead (index checks on every store, see ssm_debug_status).
 """
 
 from __future__ import annotations
@@ -13,7 +15,7 @@ import threading
 
 from . import build as _build
 
-SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT = range(5)
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_BOUNDS = range(6)
 SSM_F32, SSM_BF16 = 0, 1
 SSM_MAX_DSTATE = 16
 SSM_MAX_CONV_WIDTH = 4
@@ -94,8 +96,12 @@ _lock = threading.Lock()
 _lib = None
 
 
+def debug_selected() -> bool:
+    return os.environ.get("SSM_SCAN_LIBRARY", "") == "debug"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.LIB_DEBUG if debug_selected() else _build.LIB
 
 
 def lib():
@@ -105,9 +111,10 @@ def lib():
         return _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB
+            debug = debug_selected()
+            path = library_path()
             if _build.stale(path):
-                _build.build()
+                _build.build(debug=debug)
             if not os.path.exists(path):
                 raise RuntimeError(f"libssmscan is missing at {path} and could not be built")
             L = ctypes.CDLL(path)
@@ -141,8 +148,14 @@ def lib():
             L.ssm_selftest_flag_wait.argtypes = [_vp, ctypes.c_size_t, ctypes.c_int, _vp]
             L.ssm_version.restype = ctypes.c_char_p
             L.ssm_version.argtypes = []
+            L.ssm_debug_status.restype = ctypes.c_int
+            L.ssm_debug_status.argtypes = [ctypes.c_int]
             _lib = L
     return _lib
+
+
+def ssm_debug_status(reset: bool = False) -> int:
+    return lib().ssm_debug_status(int(reset))
 
 
 def status_string(code: int) -> str:

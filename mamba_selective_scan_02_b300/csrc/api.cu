@@ -504,8 +504,27 @@ const char *ssm_status_string(ssm_status s) {
         case SSM_ERR_UNSUPPORTED: return "unsupported by this build";
         case SSM_ERR_CUDA: return "CUDA error";
         case SSM_ERR_TIMEOUT: return "device-side wait timed out";
+        case SSM_ERR_BOUNDS: return "debug build: a store outside its buffer was skipped";
     }
     return "unknown status";
+}
+
+ssm_status ssm_debug_status(int reset) {
+#ifdef SSM_DEBUG
+    if (cudaDeviceSynchronize() != cudaSuccess) return SSM_ERR_CUDA;
+    const int words[] = {ssm::debug_word_conv(reset != 0), ssm::debug_word_step(reset != 0),
+                         ssm::debug_word_bwd(reset != 0), ssm::debug_word_fwd(reset != 0),
+                         ssm::debug_word_ssd(reset != 0)};
+    ssm_status st = SSM_OK;
+    for (int w : words) {
+        if (w < 0) return SSM_ERR_CUDA;
+        if (w != 0 && st == SSM_OK) st = SSM_ERR_BOUNDS;
+    }
+    return st;
+#else
+    (void)reset;
+    return SSM_ERR_UNSUPPORTED;
+#endif
 }
 
 ssm_status ssm_bench_mufu_ex2(float *sink, int blocks, int iters, ssm_stream_t stream) {

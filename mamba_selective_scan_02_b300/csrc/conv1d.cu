@@ -138,11 +138,11 @@ conv1d_kernel(const ConvArgs a) {
             out[i] = activate<T, SILU>(acc);
         }
         if (VEC) {
-            Vec8<T>::store(u + t, out);
+            if (in_range(row * L + t, 8, rows * L)) Vec8<T>::store(u + t, out);
         } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                if (t + i < L) u[t + i] = IO<T>::from_f(out[i]);
+                if (t + i < L && in_range(row * L + t + i, 1, rows * L)) u[t + i] = IO<T>::from_f(out[i]);
         }
     }
 
@@ -150,7 +150,7 @@ conv1d_kernel(const ConvArgs a) {
     if (H > 0 && a.state_out && seg == segs - 1 && lane < H) {
         T *so = static_cast<T *>(a.state_out) + row * H;
         const int64_t s = L - H + lane;
-        so[lane] = s >= 0 ? x[s] : (sin ? sin[H + s] : IO<T>::from_f(0.f));
+        if (in_range(row * H + lane, 1, rows * H)) so[lane] = s >= 0 ? x[s] : (sin ? sin[H + s] : IO<T>::from_f(0.f));
     }
 }
 
@@ -298,10 +298,10 @@ conv1d_stream_kernel(const ConvArgs a) {
                     out[2 * m] = acc.x;
                     out[2 * m + 1] = acc.y;
                 }
-                Raw8<T>::store(u + t, out);
+                if (in_range((int64_t)pos.row * L + t, 8, a.batch * a.dim * L)) Raw8<T>::store(u + t, out);
                 // the lane holding the row's last 8 inputs (L % 8 == 0, so L >= 8 > H)
                 // leaves the final carried inputs from its registers
-                if (H > 0 && a.state_out && t + 8 == L) {
+                if (H > 0 && a.state_out && t + 8 == L && in_range((int64_t)pos.row * H, H, a.batch * a.dim * H)) {
                     T *so = static_cast<T *>(a.state_out) + (int64_t)pos.row * H;
 #pragma unroll
                     for (int i = 0; i < H; ++i) so[i] = IO<T>::from_f(xv[8 - H + i]);
@@ -374,8 +374,8 @@ conv1d_step8_kernel(const ConvStepArgs a) {
             acc = fmaf(wf[c * W + H], xin[c], acc);
             out[c] = activate<T, SILU>(acc);
         }
-        Raw8<T>::store(static_cast<T *>(a.u) + c0, out);
-        if (H > 0) {
+        if (in_range(c0, 8, a.batch * a.dim)) Raw8<T>::store(static_cast<T *>(a.u) + c0, out);
+        if (H > 0 && in_range(c0 * H, 8 * H, a.batch * a.dim * H)) {
             // the state drops its oldest input and appends this token's, moved
             // as the loaded bits
             uint4 nw[SW > 0 ? SW : 1];
@@ -410,7 +410,8 @@ conv1d_step_kernel(const ConvStepArgs a) {
     float acc = a.bias ? __ldg(a.bias + d) : 0.f;
 #pragma unroll
     for (int k = 0; k < W; ++k) acc = fmaf(__ldg(a.w + d * W + k), win[k], acc);
-    static_cast<T *>(a.u)[c] = IO<T>::from_f(activate<T, SILU>(acc));
+    if (in_range(c, 1, a.batch * a.dim)) static_cast<T *>(a.u)[c] = IO<T>::from_f(activate<T, SILU>(acc));
+    if (!in_range(c * H, H, a.batch * a.dim * H)) return;
 #pragma unroll
     for (int k = 0; k + 1 < H; ++k) st[k] = IO<T>::from_f(win[k + 1]);
     if (H > 0) st[H - 1] = xin;
@@ -509,5 +510,7 @@ cudaError_t conv_launch(const ConvArgs &a, bool bf16, cudaStream_t stream) {
 cudaError_t conv_step_launch(const ConvStepArgs &a, bool bf16, cudaStream_t stream) {
     return bf16 ? launch_step_t<__nv_bfloat16>(a, stream) : launch_step_t<float>(a, stream);
 }
+
+SSM_DEBUG_WORD_READER(debug_word_conv)
 
 }  // namespace ssm

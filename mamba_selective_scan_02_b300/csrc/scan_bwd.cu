@@ -194,8 +194,10 @@ bwd_ckpt_kernel(const BwdArgs a) {
         for (int t0 = tb; t0 < te; t0 += TS) {
             // the state entering this tile is its checkpoint
             float4 *ck = reinterpret_cast<float4 *>(a.ckpt) + ((size_t)it.grp * a.ntiles + t0 / TS) * 64;
-            ck[lane] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
-            ck[32 + lane] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
+            if (in_range(((int64_t)it.grp * a.ntiles + t0 / TS) * 64, 64, (int64_t)a.groups * a.ntiles * 64)) {
+                ck[lane] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+                ck[32 + lane] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
+            }
 
             __syncwarp();
             store_rows<T, NP>(Bs, cur.b, N, lane);
@@ -239,7 +241,7 @@ bwd_ckpt_kernel(const BwdArgs a) {
             }
         }
         if (it.k + 1 < K) {
-            if (live) {
+            if (live && in_range(((int64_t)it.b * D + d) * N, N, (int64_t)a.batch * D * N)) {
                 float *dst = a.carry_fwd + ((size_t)it.b * D + d) * N;
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) {
@@ -565,7 +567,7 @@ bwd_rev_kernel(const BwdArgs a) {
             // one of dB / dC, every state); du, dΔraw, dz out
             {
                 const int t = lane & 15, m = lane >> 4;
-                if (t0 + t < L) {
+                if (t0 + t < L && in_range((int64_t)it.b * N * L + t0 + t, (int64_t)(N - 1) * L + 1, (int64_t)a.batch * N * L)) {
                     float *dst = (m ? a.dC : a.dB) + (size_t)it.b * N * L + t0 + t;
                     for (int n = 0; n < N; ++n) atomicAdd(dst + (size_t)n * L, sm.acc[(t * 2 + m) * NP + n]);
                 }
@@ -576,7 +578,7 @@ bwd_rev_kernel(const BwdArgs a) {
 #pragma unroll
                 for (int i = 0; i < OWN; ++i) {
                     const int j = OWN * g + i, t = t0 + j;
-                    if (t < L) {
+                    if (t < L && in_range((int64_t)rowoff + t, 1, (int64_t)a.batch * D * L)) {
                         gdu[t] = IO<T>::from_f(sm.Odu[c * TSP + j]);
                         gdd[t] = IO<T>::from_f(sm.Odd[c * TSP + j]);
                         if (gdz) gdz[t] = IO<T>::from_f(sm.Odz[c * TSP + j]);
@@ -588,7 +590,7 @@ bwd_rev_kernel(const BwdArgs a) {
 
         // ---- item end: hand the adjoint on, or write dh0; add the sums
         if (it.k > 0) {
-            if (live) {
+            if (live && in_range(((int64_t)it.b * D + d) * N, N, (int64_t)a.batch * D * N)) {
                 float *dst = a.carry_rev + ((size_t)it.b * D + d) * N;
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) {
@@ -599,7 +601,7 @@ bwd_rev_kernel(const BwdArgs a) {
             }
             __syncwarp();
             if (lane == 0) flag_release(a.flags_rev + it.grp, r + 1);
-        } else if (a.dh0 && live) {
+        } else if (a.dh0 && live && in_range(((int64_t)it.b * D + d) * N, N, (int64_t)a.batch * D * N)) {
             float *dst = a.dh0 + ((size_t)it.b * D + d) * N;
 #pragma unroll
             for (int q = 0; q < NQ; ++q) {
@@ -608,7 +610,7 @@ bwd_rev_kernel(const BwdArgs a) {
                 if (n + 1 < N) dst[n + 1] = lam[q].y;
             }
         }
-        if (live) {
+        if (live && in_range((int64_t)d * N, N, (int64_t)D * N)) {
 #pragma unroll
             for (int q = 0; q < NQ; ++q) {
                 const int n = SPT * g + 2 * q;
@@ -698,5 +700,7 @@ cudaError_t bwd_launch(const BwdArgs &a, bool bf16, cudaStream_t st) {
     if (bf16) return a.dstate <= 8 ? dispatch_bwd<__nv_bfloat16, 1>(a, vec, st) : dispatch_bwd<__nv_bfloat16, 2>(a, vec, st);
     return a.dstate <= 8 ? dispatch_bwd<float, 1>(a, vec, st) : dispatch_bwd<float, 2>(a, vec, st);
 }
+
+SSM_DEBUG_WORD_READER(debug_word_bwd)
 
 }  // namespace ssm

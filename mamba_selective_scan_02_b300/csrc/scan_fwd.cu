@@ -550,7 +550,7 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     T *gy = static_cast<T *>(a.y);
                     for (int i = lane; i < CPW * kTT; i += 32) {
                         const int tt = i / CPW, cc = i % CPW, dch = it.d0 + cc, t = t0 + tt;
-                        if (dch < D && t < it.t_end)
+                        if (dch < D && t < it.t_end && in_range(((int64_t)it.b * D + dch) * L + t, 1, (int64_t)a.batch * D * L))
                             gy[((size_t)it.b * D + dch) * L + t] = out[(tt / 8) * (CPW * 8) + cc * 8 + (tt % 8)];
                     }
                 }
@@ -567,7 +567,7 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             const bool last = it.k == K - 1;
             if (last) dst = a.hL ? a.hL + ((size_t)it.b * D + d) * N : nullptr;
             else if (chained) dst = a.carry + ((size_t)it.b * D + d) * N;
-            if (dst && live) {
+            if (dst && live && in_range(((int64_t)it.b * D + d) * N, N, (int64_t)a.batch * D * N)) {
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) {
                     const int n = SPT * g + 2 * q;
@@ -589,7 +589,8 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     const int n = SPT * g + 2 * q + j;
                     const float av = j ? A2[q].y : A2[q].x;
                     const float hv = j ? h[q].y : h[q].x;
-                    if (n < N)
+                    if (n < N && in_range((((int64_t)it.b * D + d) * (K - 1) + it.k) * N + n, 1,
+                                          (int64_t)a.batch * D * (K - 1) * N))
                         a.agg[(((size_t)it.b * D + d) * (K - 1) + it.k) * N + n] = make_float2(ex2(av * dsum), hv);
                 }
             }
@@ -909,7 +910,8 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             }
             if (CK) {  // the state entering this 16-token tile is its checkpoint
                 const int tk = t0 + 16 * hh;
-                if (tk < L) {
+                if (tk < L && in_range(((int64_t)it.grp * a.ckpt_tiles + tk / 16) * 64, 64,
+                                       (int64_t)a.groups * a.ckpt_tiles * 64)) {
                     float4 *ck = reinterpret_cast<float4 *>(a.ckpt) + ((size_t)it.grp * a.ckpt_tiles + tk / 16) * 64;
                     ck[lane] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
                     ck[32 + lane] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
@@ -1041,7 +1043,8 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                     const int n = SPT * g + 2 * q + j;
                     const float av = j ? A2[q].y : A2[q].x;
                     const float hv = j ? h[q].y : h[q].x;
-                    if (n < N)
+                    if (n < N && in_range((((int64_t)it.b * D + d) * (K - 1) + it.k) * N + n, 1,
+                                          (int64_t)a.batch * D * (K - 1) * N))
                         a.agg[(((size_t)it.b * D + d) * (K - 1) + it.k) * N + n] = make_float2(ex2(av * dsum), hv);
                 }
             }
@@ -1052,7 +1055,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             const bool last = it.k == K - 1;
             if (last) dst = (!CK && a.hL) ? a.hL + ((size_t)it.b * D + d) * N : nullptr;
             else if (chained) dst = a.carry + ((size_t)it.b * D + d) * N;
-            if (dst && live) {
+            if (dst && live && in_range(((int64_t)it.b * D + d) * N, N, (int64_t)a.batch * D * N)) {
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) {
                     const int n = SPT * g + 2 * q;
@@ -1091,7 +1094,8 @@ __global__ void __launch_bounds__(256) widen_bc_kernel(const ScanArgs a) {
     __syncthreads();
     for (int i = threadIdx.x; i < 2 * 32 * np; i += blockDim.x) {
         const int m = i / (32 * np), tt = (i / np) % 32, n = i % np, t = t0 + tt;
-        if (t < L) (m ? a.Ct : a.Bt)[((size_t)b * L + t) * np + n] = tile[m][n][tt];
+        if (t < L && in_range(((int64_t)b * L + t) * np + n, 1, (int64_t)a.batch * L * np))
+            (m ? a.Ct : a.Bt)[((size_t)b * L + t) * np + n] = tile[m][n][tt];
     }
 }
 
@@ -1110,6 +1114,7 @@ __global__ void carry_kernel(const ScanArgs a) {
     const int n = (int)(i % N);
     const int K = a.nchunks;
     const float2 *__restrict__ agg = a.agg + bd * (K - 1) * N + n;
+    if (!in_range((int64_t)(bd * K * N + n), (int64_t)(K - 1) * N + 1, (int64_t)total * K)) return;
     float *__restrict__ carry = a.carry + bd * K * N + n;
     float h = a.h0 ? a.h0[i] : 0.f;
     carry[0] = h;
@@ -1356,5 +1361,7 @@ cudaError_t scan_launch(const ScanArgs &a, bool bf16, cudaStream_t st) {
     }
     return bf16 ? dispatch_split<__nv_bfloat16>(maps, a, sp, tma, st) : dispatch_split<float>(maps, a, sp, tma, st);
 }
+
+SSM_DEBUG_WORD_READER(debug_word_fwd)
 
 }  // namespace ssm

@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
                 break;
             }
         }
-        if (a.hL) {
+        if (a.hL && in_range(((int64_t)b * H + h) * P * NS, P * NS, (int64_t)a.batch * H * P * NS)) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) a.hL[(((size_t)b * H + h) * P + 32 * hf + j) * NS + row] = S[j];
         }
@@ -596,5 +596,7 @@ cudaError_t ssd_launch(const SsdArgs &a, cudaStream_t st) {
     ssd_kernel<<<a.batch * a.nheads, kThreads, kSmemBytes, st>>>(maps, a);
     return cudaGetLastError();
 }
+
+SSM_DEBUG_WORD_READER(debug_word_ssd)
 
 }  // namespace ssm

@@ -228,6 +228,42 @@ __device__ __forceinline__ void bulk_wait_read1() {
 }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// ---------------------------------------------------------------- debug build
+// Built with -DSSM_DEBUG, every global store checks its element range against
+// the buffer it writes: a range outside is skipped and recorded (the first one
+// wins) in this source file's debug word, which the host reads through
+// ssm_debug_status.  Without SSM_DEBUG the check is `true` and compiles away.
+#ifdef SSM_DEBUG
+static __device__ int g_ssm_debug_word;
+#endif
+__device__ __forceinline__ bool in_range(int64_t first, int64_t count, int64_t size) {
+#ifdef SSM_DEBUG
+    if (first >= 0 && count >= 0 && first + count <= size) return true;
+    atomicCAS(&g_ssm_debug_word, 0, 5);   // SSM_ERR_BOUNDS
+    return false;
+#else
+    (void)first, (void)count, (void)size;
+    return true;
+#endif
+}
+// Defines `int NAME(bool reset)`, the host's reader of this source file's debug
+// word (always 0 without SSM_DEBUG).
+#ifdef SSM_DEBUG
+#define SSM_DEBUG_WORD_READER(NAME)                                              \
+    int NAME(bool reset) {                                                       \
+        int v = 0;                                                               \
+        if (cudaMemcpyFromSymbol(&v, g_ssm_debug_word, sizeof(int)) != cudaSuccess) return -1; \
+        if (reset) {                                                             \
+            const int z = 0;                                                     \
+            if (cudaMemcpyToSymbol(g_ssm_debug_word, &z, sizeof(int)) != cudaSuccess) return -1; \
+        }                                                                        \
+        return v;                                                                \
+    }
+#else
+#define SSM_DEBUG_WORD_READER(NAME) \
+    int NAME(bool) { return 0; }
+#endif
+
 // Records the first device-side error in the workspace status word.
 __device__ __forceinline__ void record_error(int *status, int code) {
     if (status) atomicCAS(status, 0, code);

@@ -181,6 +181,13 @@ int bwd_cpw(int64_t dstate);             // channels per warp of the backward ke
 constexpr int kBwdTile = 16;             // tokens per checkpoint / recompute tile
 constexpr int kBwdChunk = 128;           // tokens per work item of the backward passes
 cudaError_t conv_step_launch(const ConvStepArgs &a, bool bf16, cudaStream_t stream);
+// Each kernel source's debug word (see in_range): the first index check that
+// failed there, 0 if none or in a release build; `reset` clears it.
+int debug_word_conv(bool reset);
+int debug_word_step(bool reset);
+int debug_word_bwd(bool reset);
+int debug_word_fwd(bool reset);
+int debug_word_ssd(bool reset);
 cudaError_t mufu_ex2_launch(float *sink, int blocks, int iters, cudaStream_t stream);
 cudaError_t flag_wait_selftest_launch(int *status, const int *flag, int polls, cudaStream_t stream);
 

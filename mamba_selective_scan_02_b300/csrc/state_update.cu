@@ -70,7 +70,8 @@ __global__ void __launch_bounds__(256) step_kernel(const StepArgs a) {
     }
 #pragma unroll
     for (int m = 1; m < NG; m <<= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
-    if (!own) return;
+    if (!own || !in_range((int64_t)(ch * N + 4 * g), N - 4 * g < 4 ? N - 4 * g : 4, (int64_t)a.batch * a.dim * N))
+        return;
     if (VEC) {
         *reinterpret_cast<float4 *>(st) = make_float4(hv[0], hv[1], hv[2], hv[3]);
     } else {
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(256) step_kernel(const StepArgs a) {
     if (g == 0) {
         float out = part + (a.Dskip ? a.Dskip[d] : 0.f) * uv;
         if (HAS_Z) out *= gate_of<T>(IO<T>::to_f(static_cast<const T *>(a.z)[ch]));
-        static_cast<T *>(a.y)[ch] = IO<T>::from_f(out);
+        if (in_range((int64_t)ch, 1, (int64_t)a.batch * a.dim)) static_cast<T *>(a.y)[ch] = IO<T>::from_f(out);
     }
 }
 
@@ -158,9 +159,9 @@ __global__ void __launch_bounds__(kStepThreads) step_wide_kernel(const StepArgs 
         }
         part += __shfl_xor_sync(0xffffffffu, part, 1);
         part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if (w >= words) continue;
+        if (w >= words || !in_range((int64_t)w * 4, 4, (int64_t)a.batch * a.dim * 16)) continue;
         __stcs(reinterpret_cast<float4 *>(a.state) + w, make_float4(h4[0], h4[1], h4[2], h4[3]));
-        if (g == 0) {
+        if (g == 0 && in_range((int64_t)w / 4, 1, (int64_t)a.batch * a.dim)) {
             float out = part + skip[i] * u;
             if (HAS_Z) out *= gate_of<T>(IO<T>::to_f(zv[i]));
             static_cast<T *>(a.y)[w / 4] = IO<T>::from_f(out);
@@ -325,8 +326,11 @@ __global__ void __launch_bounds__(kStreamCh) step_stream_kernel(const StepArgs a
         __syncthreads();
         if (tid == 0) {
             const size_t ch0 = (size_t)tile * kStreamCh;
-            bulk_store(a.state + ch0 * 16, st + S::off_h, kStreamCh * 64);
-            bulk_store(static_cast<T *>(a.y) + ch0, st + S::off_y, kStreamCh * S::ES);
+            const int64_t chans = (int64_t)a.batch * a.dim;
+            if (in_range((int64_t)ch0 * 16, kStreamCh * 16, chans * 16))
+                bulk_store(a.state + ch0 * 16, st + S::off_h, kStreamCh * 64);
+            if (in_range((int64_t)ch0, kStreamCh, chans))
+                bulk_store(static_cast<T *>(a.y) + ch0, st + S::off_y, kStreamCh * S::ES);
             bulk_commit();
         }
     }
@@ -433,5 +437,7 @@ cudaError_t step_launch(const StepArgs &a, bool bf16, cudaStream_t st) {
     if (wide) return bf16 ? wide_dispatch<__nv_bfloat16>(a, st) : wide_dispatch<float>(a, st);
     return bf16 ? step_ng<__nv_bfloat16>(a, st) : step_ng<float>(a, st);
 }
+
+SSM_DEBUG_WORD_READER(debug_word_step)
 
 }  // namespace ssm
