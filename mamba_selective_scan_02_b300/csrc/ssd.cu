@@ -28,12 +28,15 @@
 // N = 128 gives both halves, which the epilogue adds).
 //
 // One CTA per (sequence, head) walks its chunks in order (the state is the
-// chain).  A control warp issues the MMAs from one lane; eight math warps —
-// two per TMEM lane quarter, each taking half the columns — form Δ and its
-// prefix sums, the weighted X, the masked block, y and the next state, and
-// hand each operand to the control warp through an mbarrier.  Inputs are
-// double-buffered, so chunk k+2's tiles load while chunk k+1 runs.
-// Shapes built: P = 64, N = 128, bf16 I/O.
+// chain).  Warp 0 issues the TMA copies and the MMAs from one lane; eight math
+// warps (warps 4 .. 11) — two per TMEM lane quarter, each taking half the
+// columns — form Δ and its prefix sums, the weighted X, the masked block, y and
+// the next state, and hand each operand to warp 0 through an mbarrier.  Warps
+// 1 .. 3 only complete warp 0's warpgroup, so that setmaxnreg can move their
+// registers to the math warpgroups (the control code needs ~100 registers
+// without spilling, the math code more than the 168 a 12-warp launch gives
+// every thread).  Inputs are double-buffered, so chunk k+2's tiles load while
+// chunk k+1 runs.  Shapes built: P = 64, N = 128, bf16 I/O.
 #include <algorithm>
 #include <cstring>
 
@@ -47,9 +50,14 @@ namespace {
 constexpr int Q = 128;                 // tokens per chunk (MMA rows)
 constexpr int P = 64;                  // head dimension
 constexpr int NS = 128;                // state size
-constexpr int kMath = 8;               // math warps
-constexpr int kCtrl = kMath;           // the control warp: MMAs from its lane 0
-constexpr int kThreads = 32 * (kMath + 1);
+constexpr int kMath = 8;               // math warps: warps 4 .. 11, two warpgroups
+constexpr int kCtrl = 0;               // the control warp: MMAs from its lane 0
+constexpr int kFirstMath = 4;          // warps 1 .. 3 only make up the control warpgroup
+constexpr int kThreads = 32 * (kFirstMath + kMath);
+// Registers per thread after the split: the control warpgroup gives up what the
+// math warpgroups take (launch: 384 threads × 168; 128 × 40 + 256 × 232 = 384 × 168).
+constexpr int kCtrlRegs = 104, kMathRegs = 200;
+static_assert(4 * 32 * kCtrlRegs + kMath * 32 * kMathRegs <= kThreads * 168, "register split");
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kStatusTimeout = 4;      // SSM_ERR_TIMEOUT
 
@@ -217,12 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
     const float Dh = a.Dskip ? a.Dskip[h] : 0.f;
     const float dbias = a.dt_bias ? a.dt_bias[h] : 0.f;
     const unsigned short *dtg = static_cast<const unsigned short *>(a.dt) + (size_t)b * L * H + h;
-    const bool math = warp < kMath;
+    const bool math = warp >= kFirstMath;
     const bool ctrl = tid == 32 * kCtrl;
+    const int lead = 32 * kFirstMath;      // the first math thread
     const int nchunks = (L + Q - 1) / Q;
 
     // math warp w: TMEM lane quarter w % 4 (rows 32·(w%4) ..), column half w / 4
-    const int qr = warp & 3, hf = (warp >> 2) & 1;
+    const int qr = warp & 3, hf = ((warp - kFirstMath) >> 2) & 1;
     const int row = 32 * qr + lane;
 
     if (tid == 0) {
@@ -237,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    if (math) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kMathRegs));
+    else asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     bool ok = true;
     int issued = 0, seen = 0;   // control thread: chunk loads issued / seen complete
 
@@ -394,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
             *reinterpret_cast<float4 *>(delta + 4 * lane) = dnext;
             *reinterpret_cast<float4 *>(cum + 4 * lane) = cnext;
         };
-        if (warp == 0) {
+        if (warp == kFirstMath) {
             fetch_dt(0);
             scan_dt(0);
             put_dt();
@@ -486,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
 
             // ---- warp 0: the next chunk's Δ and prefix sums while Y1 runs, stored
             // once every math warp is past its masked block (the last reader)
-            if (warp == 0 && ck + 1 < nchunks) {
+            if (warp == kFirstMath && ck + 1 < nchunks) {
                 scan_dt(ck + 1);
                 if (!mbar_wait_bounded(m_ready, par, kWaitLimit)) ok = false;
                 __syncwarp();
@@ -530,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
             }
             // the next chunk's Δ and prefix sums are visible; stop together on a failure
             if (math_sync_or(!ok)) {
-                if (tid == 0) *fail_flag = 1;
+                if (tid == lead) *fail_flag = 1;
                 break;
             }
         }

@@ -73,7 +73,7 @@ def algorithmic_bytes_ssd(batch: int, seqlen: int, nheads: int, headdim: int, ds
     return n
 
 
-def flops_ssd(batch: int, seqlen: int, nheads: int, headdim: int, dstate: int, chunk: int = 64) -> int:
+def flops_ssd(batch: int, seqlen: int, nheads: int, headdim: int, dstate: int, chunk: int = 128) -> int:
     """Multiply-add FLOPs of the chunked SSD algorithm at chunk length Q: per
     chunk and head, the causal half of C·Bᵀ (Q²·N) and of its product with X
     (Q²·P), the inherited state's read-out C·Sᵀ (2·Q·N·P) and the chunk's state
