@@ -604,8 +604,9 @@ def run_ours(args):
         si = make_ssd_inputs(sb, sL, sH, sP, sN, seed=51, device=dev)
         sy = torch.empty_like(si["x"])
         shL = torch.empty((sb, sH, sP, sN), dtype=torch.float32, device=dev)
+        sws = torch.empty(api.ssd_workspace_bytes(sb, sL, sH, sP, sN), dtype=torch.uint8, device=dev)
         sp = api.ssd_params(si["x"], si["dt"], si["A"], si["B"], si["C"], si["D"], si["dt_bias"], None,
-                            y=sy, hL=shL)
+                            y=sy, hL=shL, workspace=sws)
         for _ in range(3):
             capi.check(capi.ssm_ssd_fwd(sp, sh), "ssm_ssd_fwd")
         tms = []
@@ -639,9 +640,10 @@ def run_ours(args):
                           "frac": stf / bf16_peak}),
             "algorithmic_bytes": sbytes, "flops": sflops, "tflops": stf,
             "tensor_path": "tcgen05.mma kind::f16 (bf16 operands, fp32 accumulators in TMEM), TMA-fed 128-token chunks",
+            "chains": "each (sequence, head) chain in segments handing the state on through the workspace",
             "l2": "L2 flushed before every launch (256 MB written, 256 MB read)"}
         out["gpu_launches"] += 33
-        del si, sy, shL
+        del si, sy, shL, sws
 
     # ---- the short convolution in front of the scan: the layer shape (sequence
     # form) and the decode batch (one token), L2 flushed before every launch

@@ -235,11 +235,27 @@ typedef struct {
     int32_t *status;                 /* device int or NULL: a bounded wait inside the kernel
                                         that ran out stores SSM_ERR_TIMEOUT here if it still
                                         holds 0 (the caller zeroes it and reads it back) */
+    void *workspace;                 /* device, 256-byte aligned, ssm_ssd_workspace_size bytes;
+                                        or NULL */
+    size_t workspace_bytes;
 } ssm_ssd_params;
 
-/* The Mamba-2 layer scan; one launch, no workspace.  The kernel's waits on
- * its own copies and products are bounded; when one runs out, y and hL are
- * incomplete and the status word (if given) says SSM_ERR_TIMEOUT. */
+/* Workspace bytes ssm_ssd_fwd uses to split each (sequence, head) chain into
+ * segments (0 for invalid sizes): a 256-byte header (a work counter), a flag
+ * per chain and one fp32 P × N state per chain, which a segment hands to the
+ * next.  With the workspace the launch takes every chain's first segment,
+ * then every chain's second, and so on, from the counter, so that the SMs
+ * stay busy to the end; without it (NULL) one CTA walks a whole chain.  Both
+ * give bit-identical results.  The call clears the counter and the flags
+ * (an asynchronous memset on the stream) before the launch. */
+size_t ssm_ssd_workspace_size(const ssm_ssd_params *p);
+
+/* The Mamba-2 layer scan: a memset of the workspace header (when a workspace
+ * is given) and one launch.  The kernel's waits on its own copies and
+ * products, and a segment's wait for the previous segment's state, are
+ * bounded; when one runs out, y and hL are incomplete and the status word (if
+ * given) says SSM_ERR_TIMEOUT.  A workspace smaller than
+ * ssm_ssd_workspace_size, or not 256-byte aligned, is SSM_ERR_INVALID_ARG. */
 ssm_status ssm_ssd_fwd(const ssm_ssd_params *p, ssm_stream_t stream);
 
 /* ------------------------------------------------------------------------

@@ -236,7 +236,7 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, h0=None, dh
 
 
 def ssd_params(x, dt, A, B, C, D=None, dt_bias=None, h0=None, *, y, hL=None,
-               dt_softplus=True, status=None) -> capi.SsdParams:
+               dt_softplus=True, status=None, workspace=None) -> capi.SsdParams:
     """Validate tensors and build the Mamba-2 scan's C parameter struct."""
     if x.dtype not in _DT:
         raise ValueError(f"unsupported I/O dtype {x.dtype}")
@@ -262,21 +262,40 @@ def ssd_params(x, dt, A, B, C, D=None, dt_bias=None, h0=None, *, y, hL=None,
     p.x, p.dt, p.A, p.B, p.C = _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C)
     p.Dskip, p.dt_bias, p.dt_softplus = _ptr(D), _ptr(dt_bias), int(bool(dt_softplus))
     p.h0, p.y, p.hL, p.status = _ptr(h0), _ptr(y), _ptr(hL), _ptr(status)
+    if workspace is not None:
+        p.workspace = workspace.data_ptr()
+        p.workspace_bytes = workspace.numel() * workspace.element_size()
     return p
 
 
+def ssd_workspace_bytes(batch, seqlen, nheads, headdim=64, dstate=128) -> int:
+    """Workspace bytes of ssm_ssd_fwd (the segment hand-off of each chain)."""
+    p = capi.SsdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate = batch, seqlen, nheads, headdim, dstate
+    n = capi.ssm_ssd_workspace_size(p)
+    if n == 0:
+        raise ValueError("invalid SSD sizes")
+    return n
+
+
 def ssd_fwd(x, dt, A, B, C, D=None, dt_bias=None, h0=None, *, dt_softplus=True, y=None, hL=None,
-            return_last_state=True, stream=None, status=None):
+            return_last_state=True, stream=None, status=None, workspace=None, split=True):
     """Mamba-2 layer scan: x (b, L, H, P), dt (b, L, H), A (H,), B, C (b, L, N).
     Returns (y (b, L, H, P), hL (b, H, P, N) fp32 or None).  `status`, an int32
     device tensor of one element, receives SSM_ERR_TIMEOUT if a bounded wait
-    inside the kernel ran out."""
+    inside the kernel ran out.  With `split` (the default) each (sequence,
+    head) chain runs as segments handing their state on through `workspace`
+    (allocated here if None); split=False runs one CTA per chain."""
     if y is None:
         y = torch.empty_like(x)
     if hL is None and return_last_state:
         b, L, H, P = x.shape
         hL = torch.empty((b, H, P, B.shape[2]), dtype=torch.float32, device=x.device)
-    p = ssd_params(x, dt, A, B, C, D, dt_bias, h0, y=y, hL=hL, dt_softplus=dt_softplus, status=status)
+    if split and workspace is None:
+        b, L, H, P = x.shape
+        workspace = torch.empty(ssd_workspace_bytes(b, L, H, P, B.shape[2]), dtype=torch.uint8, device=x.device)
+    p = ssd_params(x, dt, A, B, C, D, dt_bias, h0, y=y, hL=hL, dt_softplus=dt_softplus, status=status,
+                   workspace=workspace if split else None)
     st = torch.cuda.current_stream(x.device).cuda_stream if stream is None else stream
     capi.check(capi.ssm_ssd_fwd(p, st), "ssm_ssd_fwd")
     return y, hL

@@ -71,6 +71,7 @@ class SsdParams(ctypes.Structure):
         ("x", _vp), ("dt", _vp), ("A", _vp), ("B", _vp), ("C", _vp),
         ("Dskip", _vp), ("dt_bias", _vp), ("dt_softplus", ctypes.c_int),
         ("h0", _vp), ("y", _vp), ("hL", _vp), ("status", _vp),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -132,6 +133,8 @@ def lib():
             L.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(BwdParams)]
             L.ssm_scan_bwd.restype = ctypes.c_int
             L.ssm_scan_bwd.argtypes = [ctypes.POINTER(BwdParams), _vp]
+            L.ssm_ssd_workspace_size.restype = ctypes.c_size_t
+            L.ssm_ssd_workspace_size.argtypes = [ctypes.POINTER(SsdParams)]
             L.ssm_ssd_fwd.restype = ctypes.c_int
             L.ssm_ssd_fwd.argtypes = [ctypes.POINTER(SsdParams), _vp]
             L.ssm_conv1d_fwd.restype = ctypes.c_int
@@ -202,6 +205,10 @@ def ssm_scan_bwd_workspace_size(p: BwdParams) -> int:
 
 def ssm_scan_bwd(p: BwdParams, stream: int) -> int:
     return lib().ssm_scan_bwd(ctypes.byref(p), stream)
+
+
+def ssm_ssd_workspace_size(p: SsdParams) -> int:
+    return lib().ssm_ssd_workspace_size(ctypes.byref(p))
 
 
 def ssm_ssd_fwd(p: SsdParams, stream: int) -> int:

@@ -378,6 +378,32 @@ ssm_status ssm_state_update(const ssm_step_params *p, ssm_stream_t stream) {
                : SSM_ERR_CUDA;
 }
 
+namespace {
+// SSD workspace: a 256-byte header (the work counter), a flag per chain, then
+// one fp32 P × N state per chain.
+struct SsdLayout {
+    size_t flags, carry, total;
+};
+SsdLayout ssd_layout(const ssm_ssd_params *p) {
+    const size_t chains = (size_t)p->batch * p->nheads;
+    SsdLayout l;
+    l.flags = 256;
+    l.carry = align256(l.flags + chains * sizeof(int));
+    l.total = l.carry + chains * (size_t)p->headdim * p->dstate * sizeof(float);
+    return l;
+}
+bool ssd_sizes_ok(const ssm_ssd_params *p) {
+    return p->batch >= 1 && p->seqlen >= 1 && p->nheads >= 1 && p->headdim >= 1 && p->dstate >= 1 &&
+           p->batch * p->nheads <= INT32_MAX / 2 && p->seqlen <= INT32_MAX / 2 && p->headdim <= 4096 &&
+           p->dstate <= 4096;
+}
+}  // namespace
+
+size_t ssm_ssd_workspace_size(const ssm_ssd_params *p) {
+    if (!p || !ssd_sizes_ok(p)) return 0;
+    return ssd_layout(p).total;
+}
+
 ssm_status ssm_ssd_fwd(const ssm_ssd_params *p, ssm_stream_t stream) {
     if (!p) return SSM_ERR_INVALID_ARG;
     if (p->batch < 1 || p->seqlen < 1 || p->nheads < 1 || p->headdim < 1 || p->dstate < 1) return SSM_ERR_INVALID_ARG;
@@ -414,7 +440,25 @@ ssm_status ssm_ssd_fwd(const ssm_ssd_params *p, ssm_stream_t stream) {
     a.y = p->y;
     a.hL = p->hL;
     a.status = p->status;
-    return ssm::ssd_launch(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    const ssm::SsdPlan plan = ssm::ssd_plan(p->batch, p->seqlen, p->nheads, p->workspace != nullptr);
+    a.seg_chunks = plan.seg_chunks;
+    a.ticket = nullptr;
+    a.flags = nullptr;
+    a.carry = nullptr;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (p->workspace) {
+        const SsdLayout l = ssd_layout(p);
+        if (p->workspace_bytes < l.total || (reinterpret_cast<uintptr_t>(p->workspace) & 255) != 0)
+            return SSM_ERR_INVALID_ARG;
+        unsigned char *ws = static_cast<unsigned char *>(p->workspace);
+        const size_t hdr = l.carry;   // counter and flags
+        if (overlaps(ws, l.total, p->y, seq) || overlaps(ws, l.total, p->x, seq)) return SSM_ERR_INVALID_ARG;
+        if (cudaMemsetAsync(ws, 0, hdr, st) != cudaSuccess) return SSM_ERR_CUDA;
+        a.ticket = reinterpret_cast<int *>(ws);
+        a.flags = reinterpret_cast<int *>(ws + l.flags);
+        a.carry = reinterpret_cast<float *>(ws + l.carry);
+    }
+    return ssm::ssd_launch(a, plan.nseg, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 ssm_status ssm_conv1d_fwd(const ssm_conv_params *p, ssm_stream_t stream) {

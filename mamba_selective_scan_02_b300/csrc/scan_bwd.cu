@@ -411,7 +411,7 @@ bwd_rev_kernel(const BwdArgs a) {
             float2 h[NQ];
 #pragma unroll
             for (int q = 0; q < NQ; ++q) h[q] = hstart[q];
-#pragma unroll 2
+#pragma unroll 4
             for (int t = 0; t < TS; ++t) {
                 const float dl = sm.Dl[c * TSP + t], du = sm.Du[c * TSP + t];
                 const float4 b0 = *reinterpret_cast<const float4 *>(sm.Bs + t * NP + SPT * g);
@@ -480,7 +480,7 @@ bwd_rev_kernel(const BwdArgs a) {
             float2 hcur[NQ];
 #pragma unroll
             for (int q = 0; q < NQ; ++q) hcur[q] = h[q];
-#pragma unroll 2
+#pragma unroll 4
             for (int t = TS - 1; t >= 0; --t) {
                 float2 hprev[NQ];
                 if (t > 0) {

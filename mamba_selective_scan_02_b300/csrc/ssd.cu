@@ -33,7 +33,7 @@
 // columns — form Δ and its prefix sums, the weighted X, the masked block, y and
 // the next state, and hand each operand to warp 0 through an mbarrier.  Warps
 // 1 .. 3 only complete warp 0's warpgroup, so that setmaxnreg can move their
-// registers to the math warpgroups (the control code needs ~100 registers
+// registers to the math warpgroups (the control code needs ~110 registers
 // without spilling, the math code more than the 168 a 12-warp launch gives
 // every thread).  Inputs are double-buffered, so chunk k+2's tiles load while
 // chunk k+1 runs.  Shapes built: P = 64, N = 128, bf16 I/O.
@@ -56,10 +56,11 @@ constexpr int kFirstMath = 4;          // warps 1 .. 3 only make up the control 
 constexpr int kThreads = 32 * (kFirstMath + kMath);
 // Registers per thread after the split: the control warpgroup gives up what the
 // math warpgroups take (launch: 384 threads × 168; 128 × 40 + 256 × 232 = 384 × 168).
-constexpr int kCtrlRegs = 104, kMathRegs = 200;
+constexpr int kCtrlRegs = 112, kMathRegs = 192;
 static_assert(4 * 32 * kCtrlRegs + kMath * 32 * kMathRegs <= kThreads * 168, "register split");
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kStatusTimeout = 4;      // SSM_ERR_TIMEOUT
+constexpr int kFlagLimit = 1 << 24;    // polls of the previous segment's flag (≈1 µs each)
 
 // Shared memory: 128-byte-swizzled slabs of 128 rows × 128 bytes (1024-byte aligned).
 constexpr int kSlab = 128 * 128;
@@ -213,7 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
     unsigned char *sm =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.x / a.nheads, h = blockIdx.x % a.nheads;
     const int L = a.seqlen, H = a.nheads;
     float *delta = reinterpret_cast<float *>(sm + kOffF), *cum = delta + Q;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
@@ -221,6 +221,16 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
     uint64_t *w_ready = bars + 6, *m_ready = bars + 7, *s_ready = bars + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
     volatile int *fail_flag = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
+    int *item_slot = reinterpret_cast<int *>(sm + kOffMisc + 8);
+    if (tid == 0) *item_slot = a.ticket ? atomicAdd(a.ticket, 1) : (int)blockIdx.x;
+    __syncthreads();
+    // the work item: segment `seg` (chunks c0 .. c0 + nchunks − 1) of the chain
+    // (b, h); segments are taken in order, every chain's first segment first
+    const int item = *item_slot, chains = a.batch * H;
+    const int seg = item / chains, chain = item % chains;
+    const int b = chain / H, h = chain % H;
+    const int c0 = seg * a.seg_chunks;
+    const int nchunks = min((L + Q - 1) / Q - c0, a.seg_chunks);
     const float Ah2 = a.A[h] * kLog2e;     // Δ·A in log2 units
     const float Dh = a.Dskip ? a.Dskip[h] : 0.f;
     const float dbias = a.dt_bias ? a.dt_bias[h] : 0.f;
@@ -228,7 +238,6 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
     const bool math = warp >= kFirstMath;
     const bool ctrl = tid == 32 * kCtrl;
     const int lead = 32 * kFirstMath;      // the first math thread
-    const int nchunks = (L + Q - 1) / Q;
 
     // math warp w: TMEM lane quarter w % 4 (rows 32·(w%4) ..), column half w / 4
     const int qr = warp & 3, hf = ((warp - kFirstMath) >> 2) & 1;
@@ -256,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
         auto issue_loads = [&](int ck) {
             const int bi = ck & 1;
             unsigned char *buf = sm + bi * kBuf;
-            const int t0 = ck * Q;
+            const int t0 = (c0 + ck) * Q;
             mbar_arrive_expect_tx(&full[bi], 5u * kSlab);
             tma_load_4d(buf + kBufX, &maps.x, &full[bi], 0, h, t0, b);
             for (int s = 0; s < 2; ++s) {
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
         };
         // chunk ck's y (over its X tile) leaves; ck + 2 then loads into that buffer
         auto store_y = [&](int ck) {
-            tma_store_4d(&maps.y, sm + (ck & 1) * kBuf + kBufX, 0, h, ck * Q, b);   // rows past L are clipped
+            tma_store_4d(&maps.y, sm + (ck & 1) * kBuf + kBufX, 0, h, (c0 + ck) * Q, b);   // rows past L are clipped
             bulk_commit();
         };
         issue_loads(0);
@@ -374,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
         auto fetch_dt = [&](int ck) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int t = ck * Q + 4 * lane + e;
+                const int t = (c0 + ck) * Q + 4 * lane + e;
                 if (t < L) dtr[e] = dtg[(size_t)t * H];
             }
         };
@@ -386,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float x = __uint_as_float((uint32_t)dtr[e] << 16) + dbias;
-                d[e] = 4 * lane + e + ck * Q < L ? (a.dt_softplus ? softplus_poly(x) : x) : 0.f;
+                d[e] = 4 * lane + e + (c0 + ck) * Q < L ? (a.dt_softplus ? softplus_poly(x) : x) : 0.f;
                 run = fmaf(d[e], Ah2, run);
                 c[e] = run;
             }
@@ -410,9 +419,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
             scan_dt(0);
             put_dt();
         }
+        // the state entering the segment: h0 (or zero) for a chain's first, else
+        // what the previous segment left in the carry once its flag is up
+        const float *sin = seg == 0 ? a.h0 : a.carry;
+        if (seg > 0) {
+            if (tid == lead && !wait_flag(a.flags + chain, seg, kFlagLimit)) ok = false;
+            math_sync();
+            (void)flag_acquire(a.flags + chain);
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            S[j] = a.h0 ? a.h0[(((size_t)b * H + h) * P + 32 * hf + j) * NS + row] : 0.f;
+            S[j] = sin ? __ldcg(sin + (((size_t)b * H + h) * P + 32 * hf + j) * NS + row) : 0.f;
         store_state();
         fence_proxy_async_smem();
         __syncwarp();
@@ -545,9 +562,21 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_kernel(const __grid_constant_
                 break;
             }
         }
-        if (a.hL && in_range(((int64_t)b * H + h) * P * NS, P * NS, (int64_t)a.batch * H * P * NS)) {
+        // a chain's last segment writes hL; the others hand the state on
+        const bool last = c0 + nchunks >= (L + Q - 1) / Q;
+        float *sout = last ? a.hL : a.carry;
+        if (sout && in_range(((int64_t)b * H + h) * P * NS, P * NS, (int64_t)a.batch * H * P * NS)) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a.hL[(((size_t)b * H + h) * P + 32 * hf + j) * NS + row] = S[j];
+            for (int j = 0; j < 32; ++j) sout[(((size_t)b * H + h) * P + 32 * hf + j) * NS + row] = S[j];
+        }
+        if (!last) {
+            // every math thread's state stores precede the flag (barrier, then a
+            // release at device scope by one thread)
+            math_sync();
+            if (tid == lead) {
+                __threadfence();
+                flag_release(a.flags + chain, seg + 1);
+            }
         }
     }
     __syncwarp();
@@ -582,7 +611,30 @@ bool make_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
 
 bool ssd_supported(int64_t headdim, int64_t dstate) { return headdim == P && dstate == NS; }
 
-cudaError_t ssd_launch(const SsdArgs &a, cudaStream_t st) {
+// Segments per chain.  One CTA per SM runs a segment at a time, so the launch
+// takes ⌈segments × chains / SMs⌉ rounds, each as long as a segment plus its
+// start: ≈2.5 chunk-times (CTA start, TMEM allocation, the first tiles' load
+// from memory and G before the pipeline is full), fitted to B300 timings of the
+// 4 × 2048 and 8 × 4096 token, 80-head layers split into 1, 2 and 4 segments.
+// The split with the fewest chunk-times wins, up to four segments.
+SsdPlan ssd_plan(int64_t batch, int64_t seqlen, int64_t nheads, bool split) {
+    const int64_t nch = (seqlen + Q - 1) / Q, chains = batch * nheads;
+    SsdPlan p{(int)nch, 1};
+    if (!split) return p;
+    const int64_t sms = sm_count();
+    double best = 1e300;
+    for (int64_t s = 1; s <= std::min<int64_t>(4, nch); ++s) {
+        const int64_t per = (nch + s - 1) / s, nseg = (nch + per - 1) / per;
+        const double t = (double)((nseg * chains + sms - 1) / sms) * ((double)per + 2.5);
+        if (t < best * 0.999) {
+            best = t;
+            p = SsdPlan{(int)per, (int)nseg};
+        }
+    }
+    return p;
+}
+
+cudaError_t ssd_launch(const SsdArgs &a, int nseg, cudaStream_t st) {
     Maps maps;
     memset(&maps, 0, sizeof(maps));
     const cuuint64_t Lb = (cuuint64_t)a.seqlen, Bb = (cuuint64_t)a.batch, Hh = (cuuint64_t)a.nheads;
@@ -604,7 +656,7 @@ cudaError_t ssd_launch(const SsdArgs &a, cudaStream_t st) {
         },
         &done);
     if (e != cudaSuccess) return e;
-    ssd_kernel<<<a.batch * a.nheads, kThreads, kSmemBytes, st>>>(maps, a);
+    ssd_kernel<<<nseg * a.batch * a.nheads, kThreads, kSmemBytes, st>>>(maps, a);
     return cudaGetLastError();
 }
 

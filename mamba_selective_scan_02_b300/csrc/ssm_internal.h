@@ -138,7 +138,17 @@ struct SsdArgs {
     void *y;                         // b × L × H × P
     float *hL;                       // b × H × P × N fp32 or null
     int *status;                     // device status word or null
+    int seg_chunks;                  // chunks per segment of a chain (all of them: one segment)
+    int *ticket;                     // work counter, zero at launch (null: item = block index)
+    int *flags;                      // b × H: segments of the chain finished, zero at launch
+    float *carry;                    // b × H × P × N fp32: the state a segment hands on
 };
+// Segments per (sequence, head) chain of the SSD kernel, and the launch's
+// work items: every chain's first segment, then every chain's second, ...
+struct SsdPlan {
+    int seg_chunks, nseg;
+};
+SsdPlan ssd_plan(int64_t batch, int64_t seqlen, int64_t nheads, bool split);
 
 // Causal depthwise convolution + bias + optional SiLU over whole sequences.
 struct ConvArgs {
@@ -175,7 +185,7 @@ cudaError_t scan_ckpt_launch(const ScanArgs &a, cudaStream_t stream);
 cudaError_t step_launch(const StepArgs &a, bool bf16, cudaStream_t stream);
 cudaError_t conv_launch(const ConvArgs &a, bool bf16, cudaStream_t stream);
 bool ssd_supported(int64_t headdim, int64_t dstate);
-cudaError_t ssd_launch(const SsdArgs &a, cudaStream_t stream);
+cudaError_t ssd_launch(const SsdArgs &a, int nseg, cudaStream_t stream);
 cudaError_t bwd_launch(const BwdArgs &a, bool bf16, cudaStream_t stream);
 int bwd_cpw(int64_t dstate);             // channels per warp of the backward kernels
 constexpr int kBwdTile = 16;             // tokens per checkpoint / recompute tile

@@ -319,6 +319,19 @@ def valid_ssd(**over):
     return p
 
 
+def test_ssd_workspace_size_and_rejections():
+    p = valid_ssd()
+    n = capi.ssm_ssd_workspace_size(p)
+    chains = 2 * 4
+    assert n == 256 + (-(-chains * 4 // 256) * 256) + chains * 64 * 128 * 4
+    assert capi.lib().ssm_ssd_workspace_size(None) == 0
+    assert capi.ssm_ssd_workspace_size(valid_ssd(batch=0)) == 0
+    small = valid_ssd(workspace=FAKE + (1 << 26), workspace_bytes=n - 1)
+    assert capi.ssm_ssd_fwd(small, None) == capi.SSM_ERR_INVALID_ARG
+    odd = valid_ssd(workspace=FAKE + (1 << 26) + 16, workspace_bytes=n)
+    assert capi.ssm_ssd_fwd(odd, None) == capi.SSM_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("over,code", [
     (dict(batch=0), capi.SSM_ERR_INVALID_ARG),
     (dict(nheads=0), capi.SSM_ERR_INVALID_ARG),

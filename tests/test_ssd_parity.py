@@ -116,3 +116,34 @@ def test_ssd_writes_nothing_past_y_and_hL(L):
     wy, wh = orc.ssd(c["x"], c["dt"], c["A"], c["B"], c["C"], Dskip=c["D"], dt_bias=c["dt_bias"], h0=c["h0"])
     check("y", y, wy)
     check("hL", hL, wh, scale=1.0 + np.abs(wh) + np.sqrt(np.mean(wh ** 2)))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("b,L,H", [(2, 300, 3), (1, 1000, 2), (3, 520, 4), (1, 128, 1)])
+@pytest.mark.parametrize("h0", [False, True])
+def test_ssd_segments_equal_whole_chains(b, L, H, h0):
+    # the segment hand-off passes the fp32 state exactly: split and unsplit
+    # launches must agree bit for bit
+    inp = make_ssd_inputs(b, L, H, seed=b * L + H, device="cuda", with_h0=h0)
+    args = (inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["dt_bias"], inp["h0"])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y1, h1 = api.ssd_fwd(*args, split=True, status=status)
+    y2, h2 = api.ssd_fwd(*args, split=False)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(y1, y2)
+    assert torch.equal(h1, h2)
+
+
+@pytest.mark.gpu
+def test_ssd_workspace_reused_across_calls():
+    # the call clears the counter and flags itself: one workspace serves calls
+    # of different sizes in a row
+    ws = torch.empty(api.ssd_workspace_bytes(2, 1000, 4), dtype=torch.uint8, device="cuda")
+    for seed, (b, L, H) in enumerate([(2, 1000, 4), (1, 700, 3), (2, 1000, 4)]):
+        inp = make_ssd_inputs(b, L, H, seed=seed, device="cuda")
+        args = (inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["dt_bias"], None)
+        y1, h1 = api.ssd_fwd(*args, workspace=ws)
+        y2, h2 = api.ssd_fwd(*args, split=False)
+        torch.cuda.synchronize()
+        assert torch.equal(y1, y2) and torch.equal(h1, h2), (b, L, H)
