@@ -32,7 +32,11 @@ def test_scan_decode_conv_ssd_replay_in_a_graph():
     si = make_ssd_inputs(1, 256, 4, seed=33, device=dev)
     sy = torch.empty_like(si["x"])
     shl = torch.empty((1, 4, 64, 128), dtype=torch.float32, device=dev)
-    pssd = api.ssd_params(si["x"], si["dt"], si["A"], si["B"], si["C"], si["D"], si["dt_bias"], None, y=sy, hL=shl)
+    # with a workspace: each chain runs as segments handing the state on (a
+    # memset of the work counter and flags, then the launch)
+    sws = torch.empty(api.ssd_workspace_bytes(1, 256, 4), dtype=torch.uint8, device=dev)
+    pssd = api.ssd_params(si["x"], si["dt"], si["A"], si["B"], si["C"], si["D"], si["dt_bias"], None, y=sy, hL=shl,
+                          workspace=sws)
 
     side = torch.cuda.Stream(dev)
     # eager reference results (and the first call of each entry point, which
