@@ -316,8 +316,8 @@ def run_ours(args):
         flush_w.zero_()
         flush_r.sum()
     plan = capi.ssm_scan_plan(p)
-    # B/C widening + scan, or widening + aggregate + carry + scan in two-pass mode
-    launches_per_step = 2 if (plan["chained"] or plan["nchunks"] == 1) else 4
+    # B/C widening + scan (chained, one chunk, or look-back alike)
+    launches_per_step = 2
 
     # MUFU ex2 peak, measured on this GPU (the roofline's exponential side)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count

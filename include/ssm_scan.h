@@ -98,15 +98,20 @@ size_t ssm_scan_workspace_size(const ssm_scan_params *p);
 /* How ssm_scan_fwd will cut this scan into work items (host-side, no GPU
  * needed).  On SSM_OK fills out[0] = tokens per chunk, out[1] = number of
  * chunks K, out[2] = 1 if chunk k starts from the state chunk k-1 hands over
- * (one scan launch) or 0 if an aggregate pass and a carry pass precompute the
- * chunks' starting states (three launches when K > 1), out[3] = number of
- * channel groups (one scanning warp each).  Every scan is preceded by one small launch
- * that widens B and C to fp32 token-major rows in the workspace.  Returns SSM_ERR_INVALID_ARG for invalid
- * sizes or a NULL out. */
+ * (chained) or 0 if, when K > 1, the chunks run at once and carry their
+ * starting states by decoupled look-back: aggregate work items scan each
+ * chunk but the last from a zero state for its pair (Π Ā, h_end) and publish
+ * it; each chunk's main item composes its predecessors' pairs from h0 in chunk
+ * order (bit for bit the same whichever predecessor the walk stops at),
+ * publishes the state it leaves and scans, out[3] = number of channel
+ * groups (one scanning warp each).  Either way the scan is one launch,
+ * preceded by one small launch that widens B and C to fp32 token-major rows
+ * in the workspace.  Returns SSM_ERR_INVALID_ARG for invalid sizes or a NULL
+ * out. */
 ssm_status ssm_scan_plan(const ssm_scan_params *p, int64_t out[4]);
 
 /* Forward selective scan: writes y and (if non-NULL) hL.  Also clears the
- * workspace status word before launching.  In chained mode the launch's warps
+ * workspace status word before launching.  With K > 1 the launch's warps
  * wait on one another (bounded spins on flags in the workspace); its grid is
  * sized to the CTAs the device holds at once, so work that occupies SMs for
  * long on another stream can delay it, and a wait that reaches its bound is

@@ -30,8 +30,8 @@ bool scan_sizes_ok(const ssm_scan_params *p) {
 
 // Workspace: a 256-byte header (status word, two work counters), then
 //   chained:  one int flag per channel group, and one b × D × N fp32 state;
-//   two-pass: per-chunk aggregates [b][D][K-1][N] (float2) and carried states
-//             [b][D][K][N] (fp32);
+//   look-back: one int flag per (channel group, chunk), per-chunk aggregates
+//             [b][D][K-1][N] (float2) and carried states [b][D][K][N] (fp32);
 // then, always, B and C widened to fp32 token-major rows [b][L][np].
 // The header and the flags are cleared before every launch.
 Layout scan_layout(const ssm_scan_params *p) {
@@ -47,8 +47,11 @@ Layout scan_layout(const ssm_scan_params *p) {
         l.zero_bytes = kHeader + flag_bytes;
         l.total = l.carry_off + align256(bdn * sizeof(float));
     } else if (l.plan.nchunks > 1) {
+        const size_t flag_bytes = align256((size_t)l.plan.groups * (size_t)l.plan.nchunks * sizeof(int));
         const size_t agg_bytes = align256(bdn * (size_t)(l.plan.nchunks - 1) * sizeof(float2));
-        l.carry_off = kHeader + agg_bytes;
+        l.agg_off = kHeader + flag_bytes;
+        l.zero_bytes = l.agg_off;
+        l.carry_off = l.agg_off + agg_bytes;
         l.total = l.carry_off + align256(bdn * (size_t)l.plan.nchunks * sizeof(float));
     }
     const size_t bt_bytes = align256((size_t)p->batch * p->seqlen * l.plan.np * sizeof(float));

@@ -24,11 +24,13 @@
 //     and chunk k of a group starts from the state chunk k-1 published
 //     (waiting on a flag, with a bounded spin): every warp stays busy until
 //     the end whatever the channel count, with no extra pass.  When there are
-//     too few groups to fill the GPU, two-pass mode cuts the sequence into
-//     chunks that run at once: an aggregate pass computes each chunk's pair
-//     (Π Ā, h_end from zero), a carry pass chains the pairs from h0 (the
-//     affine composition of first-principles page, "The hardware-aware scan"),
-//     and the main pass rescans every chunk from its carried state.
+//     too few groups to fill the GPU, look-back mode cuts the sequence into
+//     chunks that run at once, in the same one launch: every warp first takes
+//     aggregate items, which walk a chunk (every chunk but the last) from a
+//     zero state and publish its pair (Π Ā, h_end), and then main items, which
+//     compose their predecessors' pairs from h0 (the affine composition of the
+//     first-principles page, "The hardware-aware scan") for the state they
+//     start from, publish the state they leave, and scan from there.
 //   * Per tile of TT tokens one lane moves u, Δraw, z (as 8-token × CPW-channel
 //     boxes) and B, C (N × TT, shared by every channel) into shared memory with
 //     TMA on an mbarrier, two stages deep; the next tile — of the same item or
@@ -163,11 +165,178 @@ struct Item {
     int grp, k, b, d0, t_begin, t_end, ntiles;
 };
 
+// ---------------------------------------------------------------- look-back carry
+// Chunks of one channel group that run at once join up through the affine
+// composition of the first-principles page ("The hardware-aware scan"): chunk
+// k's pair (P_k, S_k) = (Π Ā, h_end from a zero state) maps the state entering
+// it to the state leaving it, h -> P_k·h + S_k.  Per (group, chunk) a flag in
+// the workspace says what is out: 0 nothing, 1 the pair (in a.agg, written by
+// the chunk's aggregate item), 2 also the state leaving the chunk (in a.carry,
+// slot k + 1, written by its main item before it scans).  In a look-back
+// launch every warp runs aggregate items (chunks 0 .. K-2) until their counter
+// runs out and then main items; main items wait only on aggregate items, which
+// wait on nothing and were all taken by running warps before any main item
+// was, so every wait ends.  A lane holds states n = SPT·g + 2q + e of channel
+// d as h[q].{x, y}.
+
+// End of chunk it.k's aggregate item, with h the state reached from zero and
+// dsum = Σ Δ over the chunk: publishes the pair (flag 1).  A2 holds A·log2(e),
+// so P = 2^(A2·ΣΔ) = exp(A·ΣΔ).  The warp barrier orders every lane's stores
+// before lane 0's release store.
+template <int SPT, int NQ>
+__device__ __forceinline__ void publish_pair(const ScanArgs &a, const Item &it, int d, bool live, int g, int lane,
+                                             const float2 (&A2)[NQ], float dsum, const float2 (&h)[NQ]) {
+    const int D = a.dim, N = a.dstate, K = a.nchunks;
+    const int64_t at = (((int64_t)it.b * D + d) * (K - 1) + it.k) * N;
+    if (live && in_range(at, N, (int64_t)a.batch * D * (K - 1) * N)) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const int n = SPT * g + 2 * q;
+            if (n < N) a.agg[at + n] = make_float2(ex2(A2[q].x * dsum), h[q].x);
+            if (n + 1 < N) a.agg[at + n + 1] = make_float2(ex2(A2[q].y * dsum), h[q].y);
+        }
+    }
+    __syncwarp();
+    if (lane == 0) flag_release(a.flags + (size_t)it.grp * K + it.k, 1);
+}
+
+// Start of chunk it.k's main item: sets h to the state entering the chunk and,
+// but for the last chunk, writes the state leaving it to a.carry; the caller
+// then releases flag 2 (release_leaving) once the item's first tile is done,
+// when those stores have long landed.  The walk goes back along the group's
+// flags to the nearest chunk whose leaving state is out (else to h0) and
+// carries that state forward through the pairs in between, oldest first, one
+// fmaf per chunk and state: whichever chunk the walk stops at, the bits are
+// those of h0 carried chunk by chunk.  Lane i reads the flag of the i-th
+// predecessor, 32 at a time, so one round trip finds the stop; the warp
+// barrier after the walk orders every lane's reads after the acquire loads
+// that saw the flags.  A wait that runs out records SSM_ERR_TIMEOUT and the
+// walk goes on with what is there.
+template <int SPT, int NQ>
+__device__ __forceinline__ void enter_chunk(const ScanArgs &a, const Item &it, int d, bool live, int g, int lane,
+                                            float2 (&h)[NQ]) {
+    constexpr unsigned FULL = 0xffffffffu;
+    const int D = a.dim, N = a.dstate, K = a.nchunks, k = it.k;
+    const bool leaves = k < K - 1;  // the state leaving the chunk is published
+    const int *fl = a.flags + (size_t)it.grp * K;
+    bool ok = true;
+    int j = -1;                     // the chunk whose leaving state the walk starts from
+    int base = k - 1;               // lane i looks at chunk base - i
+    bool own = !leaves;             // the chunk's own pair is out
+    for (int polls = 1;; ++polls) {
+        if (!own) own = __all_sync(FULL, flag_acquire(fl + k) >= 1);
+        bool found = base < 0;
+        if (!found) {
+            const int m = base - lane;
+            const int f = m >= 0 ? flag_acquire(fl + m) : 1;  // before chunk 0: h0
+            const unsigned two = __ballot_sync(FULL, m >= 0 && f == 2);
+            const unsigned none = __ballot_sync(FULL, f == 0);
+            const unsigned nearer = two ? (two & (0u - two)) - 1u : FULL;  // lanes before the first 2
+            if (!(none & nearer)) {
+                if (two) {
+                    j = base - (__ffs(two) - 1);
+                    found = true;
+                } else {
+                    base -= 32;  // every pair in this window is out: look further back
+                    found = base < 0;
+                    if (!found) continue;
+                }
+            }
+        }
+        if (found && own) break;
+        if (polls >= kFlagLimit) {
+            ok = false;
+            j = -1;
+            break;
+        }
+        __nanosleep(64);
+    }
+    __syncwarp();
+    const size_t bd = (size_t)it.b * D + d;
+    const int64_t agg_size = (int64_t)a.batch * D * (K - 1) * N;
+    // the chunk's own pair first: its loads do not wait on the walk's
+    float2 P[NQ], S[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        P[q] = make_float2(1.f, 1.f);
+        S[q] = make_float2(0.f, 0.f);
+    }
+    const float2 *own_pair = a.agg + (bd * (K - 1) + k) * N;
+    const bool use_own = leaves && live && in_range((int64_t)(bd * (K - 1) + k) * N, N, agg_size);
+    if (use_own) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const int n = SPT * g + 2 * q;
+            if (n < N) {
+                const float2 ps = __ldcg(own_pair + n);
+                P[q].x = ps.x;
+                S[q].x = ps.y;
+            }
+            if (n + 1 < N) {
+                const float2 ps = __ldcg(own_pair + n + 1);
+                P[q].y = ps.x;
+                S[q].y = ps.y;
+            }
+        }
+    }
+    const float *src = nullptr;
+    if (j >= 0) src = a.carry + (bd * K + j + 1) * N;
+    else if (a.h0) src = a.h0 + bd * N;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        const int n = SPT * g + 2 * q;
+        float hx = 0.f, hy = 0.f;
+        if (src && live) {
+            if (n < N) hx = __ldcg(src + n);
+            if (n + 1 < N) hy = __ldcg(src + n + 1);
+        }
+        h[q] = make_float2(hx, hy);
+    }
+#pragma unroll 1
+    for (int m = j + 1; m < k; ++m) {  // h <- P_m·h + S_m
+        if (!live || !in_range((int64_t)(bd * (K - 1) + m) * N, N, agg_size)) break;
+        const float2 *pr = a.agg + (bd * (K - 1) + m) * N;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const int n = SPT * g + 2 * q;
+            if (n < N) {
+                const float2 ps = __ldcg(pr + n);
+                h[q].x = fmaf(ps.x, h[q].x, ps.y);
+            }
+            if (n + 1 < N) {
+                const float2 ps = __ldcg(pr + n + 1);
+                h[q].y = fmaf(ps.x, h[q].y, ps.y);
+            }
+        }
+    }
+    const int64_t ct = ((int64_t)bd * K + k + 1) * N;
+    if (use_own && in_range(ct, N, (int64_t)a.batch * D * K * N)) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const int n = SPT * g + 2 * q;
+            if (n < N) a.carry[ct + n] = fmaf(P[q].x, h[q].x, S[q].x);
+            if (n + 1 < N) a.carry[ct + n + 1] = fmaf(P[q].y, h[q].y, S[q].y);
+        }
+    }
+    if (!ok && lane == 0) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
+}
+
+// Flag 2 for a main item's chunk after enter_chunk wrote its leaving state
+// (the warp barrier orders every lane's stores before lane 0's release).
+__device__ __forceinline__ void release_leaving(const ScanArgs &a, const Item &it, int lane) {
+    if (it.k >= a.nchunks - 1) return;
+    __syncwarp();
+    if (lane == 0) flag_release(a.flags + (size_t)it.grp * a.nchunks + it.k, 2);
+}
+
+// One pass of the single-warp scan over its work items; false if a wait ran out.
 // MODE 0: scan writing y (and hL after the last chunk).
-// MODE 1: chunk aggregate (Π Ā, h_end from zero) for chunks 0..K-2 (two-pass).
-template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, int MODE, bool ZOH>
-__global__ void __launch_bounds__(32, 1)
-scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
+// MODE 1: chunk aggregate (Π Ā, h_end from zero) for chunks 0..K-2, each
+//         published for the look-back (publish_pair).
+// LBK: the pass runs in a look-back launch (scan_lb_kernel): a MODE 0 pass
+//      finds every chunk's start state by look-back (enter_chunk).
+template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, int MODE, bool ZOH, bool LBK>
+__device__ __forceinline__ bool scan_pass(const Maps &maps, const ScanArgs &a) {
     using S = WTile<T, SPT, NG>;
     constexpr int CPW = S::CPW, NB8 = S::NB8, NQ = SPT / 2;
     constexpr unsigned FULL = 0xffffffffu;
@@ -203,13 +372,6 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
         if (lane == 0) t = atomicAdd(ticket, 1);
         return __shfl_sync(FULL, t, 0);
     };
-
-    if (TMA && lane == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
 
     constexpr uint32_t bc_bytes = S::BC;
     auto stage = [&](int s) { return smem + s * S::BUF; };
@@ -255,7 +417,7 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     };
 
     int cur = grab();
-    if (cur >= items) return;
+    if (cur >= items) return true;
     int nxt = grab();
     Item it = item_of(cur);
     int s = 0;                 // stage holding the current tile
@@ -287,7 +449,9 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
         if (MODE == 0) {
             const float *src = nullptr;
             bool cg = false;  // read through L2 only: another SM wrote it during this launch
-            if (it.k == 0) {
+            if (LBK) {
+                enter_chunk<SPT, NQ>(a, it, d, live, g, lane, h);
+            } else if (it.k == 0) {
                 src = a.h0 ? a.h0 + ((size_t)it.b * D + d) * N : nullptr;
             } else if (chained) {
                 if (lane == 0 && !wait_flag(a.flags + it.grp, it.k, kFlagLimit))
@@ -295,9 +459,6 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 __syncwarp();
                 (void)flag_acquire(a.flags + it.grp);  // every lane orders its reads after the hand-off
                 src = a.carry + ((size_t)it.b * D + d) * N;
-                cg = true;
-            } else {
-                src = a.carry + (((size_t)it.b * D + d) * K + it.k) * N;
                 cg = true;
             }
             if (src && live) {
@@ -558,6 +719,7 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             }
             __syncwarp();  // this tile's B/C rows and stage are free again
             s ^= 1;
+            if (LBK && MODE == 0 && tile == 0) release_leaving(a, it, lane);
         }
         if (failed) break;
 
@@ -581,19 +743,8 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 __syncwarp();
                 if (lane == 0) flag_release(a.flags + it.grp, it.k + 1);
             }
-        } else if (live) {
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int n = SPT * g + 2 * q + j;
-                    const float av = j ? A2[q].y : A2[q].x;
-                    const float hv = j ? h[q].y : h[q].x;
-                    if (n < N && in_range((((int64_t)it.b * D + d) * (K - 1) + it.k) * N + n, 1,
-                                          (int64_t)a.batch * D * (K - 1) * N))
-                        a.agg[(((size_t)it.b * D + d) * (K - 1) + it.k) * N + n] = make_float2(ex2(av * dsum), hv);
-                }
-            }
+        } else {
+            publish_pair<SPT, NQ>(a, it, d, live, g, lane, A2, dsum, h);
         }
 
         cur = nxt;
@@ -603,6 +754,45 @@ scan_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     }
     if (failed) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
     if (TMA && MODE == 0 && lane == 0) bulk_wait0();
+    return !failed;
+}
+
+template <typename T, int SPT, int NG, bool TMA>
+__device__ __forceinline__ void scan_init_bars(bool again) {
+    using S = WTile<T, SPT, NG>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::off_bar);
+    if (TMA && threadIdx.x == 0) {
+        if (again) {
+            mbar_inval(&bar[0]);
+            mbar_inval(&bar[1]);
+        }
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+}
+
+// A scan whose chunks are chained or single.
+template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, bool ZOH>
+__global__ void __launch_bounds__(32, 1)
+scan_kernel(const __grid_constant__ Maps maps, const __grid_constant__ ScanArgs a) {
+    scan_init_bars<T, SPT, NG, TMA>(false);
+    (void)scan_pass<T, SPT, NG, HAS_Z, TMA, 0, ZOH, false>(maps, a);
+}
+
+// A scan whose chunks run at once, joined by look-back: every warp runs
+// aggregate items until they run out, then main items.  Between the two
+// passes the warp's stage barriers start afresh (every load it issued has
+// been waited for).
+template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, bool ZOH>
+__global__ void __launch_bounds__(32, 1)
+scan_lb_kernel(const __grid_constant__ Maps maps, const __grid_constant__ ScanArgs a) {
+    scan_init_bars<T, SPT, NG, TMA>(false);
+    if (!scan_pass<T, SPT, NG, false, TMA, 1, ZOH, true>(maps, a)) return;
+    scan_init_bars<T, SPT, NG, TMA>(true);
+    (void)scan_pass<T, SPT, NG, HAS_Z, TMA, 0, ZOH, true>(maps, a);
 }
 
 // ------------------------------------------------------- warp-specialised passes
@@ -650,14 +840,18 @@ template <typename T> struct WsTile {
 
 constexpr int kWsFirst = 1, kWsLast = 2, kWsEnd = 4;  // header flags
 
+// One pass of a producer / consumer pair over its work items; false if a wait
+// ran out.
 // WM = 0: the main pass (y, and hL or the hand-off after each item).
-// WM = 1: the two-pass aggregate pass — each chunk but the last from a zero
-//         state, (Π Ā, h_end) into a.agg; no read-out, no y, no C.
+// WM = 1: the aggregate pass — each chunk but the last from a zero state,
+//         (Π Ā, h_end) published for the look-back (publish_pair); no
+//         read-out, no y, no C.
 // WM = 2: the backward's checkpoint pass — the state at every 16-token tile
 //         start into a.ckpt; no read-out, no y, no C.
-template <typename T, bool HAS_Z, bool ZOH, int WM>
-__global__ void __launch_bounds__(256, 2)
-scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
+// LBK: the pass runs in a look-back launch (scan_ws_lb_kernel): a main pass
+//      finds every chunk's start state by look-back (enter_chunk).
+template <typename T, bool HAS_Z, bool ZOH, int WM, bool LBK>
+__device__ __forceinline__ bool ws_pass(const Maps &maps, const ScanArgs &a) {
     constexpr bool OUTY = WM == 0, AG = WM == 1, CK = WM == 2;
     using S = WsTile<T>;
     using Wt = WTile<T, 8, 2>;
@@ -694,14 +888,6 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
         return reinterpret_cast<float4 *>(smem + S::off_trm + (2 * slot + which) * S::TRM);
     };
 
-    if (role == 0 && lane == 0) {
-        mbar_init(&tma_full[0], 1);
-        mbar_init(&tma_full[1], 1);
-        for (int i = 2; i < 8; ++i) mbar_init(&bar[i], kWsArrivals);
-        fence_mbar_init();
-    }
-    __syncthreads();
-
     if (role == 1) {
         // ================================================================ producer
         const int c = lane >> 1, hg = lane & 1;  // channel, which 8-token block of a half tile
@@ -734,7 +920,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
         int cur = grab();
         if (cur >= items) {
             publish_end(0);
-            return;
+            return true;
         }
         Item it = item_of(cur);
         int tile = 0;
@@ -824,7 +1010,7 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             tile = ntile;
         }
         if (!ok) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
-        return;
+        return ok;
     }
 
     // ==================================================================== consumer
@@ -866,6 +1052,8 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
             bool cg = false;  // read through L2 only: another SM wrote it during this launch
             if (AG) {
                 // every aggregate starts from a zero state
+            } else if (LBK) {
+                enter_chunk<SPT, NQ>(a, it, d, live, g, lane, h);
             } else if (it.k == 0) {
                 src = a.h0 ? a.h0 + ((size_t)it.b * D + d) * N : nullptr;
             } else if (chained) {
@@ -874,9 +1062,6 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
                 __syncwarp();
                 (void)flag_acquire(a.flags + it.grp);  // every lane orders its reads after the hand-off
                 src = a.carry + ((size_t)it.b * D + d) * N;
-                cg = true;
-            } else {
-                src = a.carry + (((size_t)it.b * D + d) * K + it.k) * N;
                 cg = true;
             }
             if (src && live) {
@@ -1034,21 +1219,9 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
         }
         __syncwarp();
         ws_arrive(&stage_empty[s]);  // this tile's B, C rows are read
-        if (AG && (hd.z & kWsLast) && live) {
-            // ---- item end (aggregate pass): the chunk's (Π Ā, h_end from zero)
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int n = SPT * g + 2 * q + j;
-                    const float av = j ? A2[q].y : A2[q].x;
-                    const float hv = j ? h[q].y : h[q].x;
-                    if (n < N && in_range((((int64_t)it.b * D + d) * (K - 1) + it.k) * N + n, 1,
-                                          (int64_t)a.batch * D * (K - 1) * N))
-                        a.agg[(((size_t)it.b * D + d) * (K - 1) + it.k) * N + n] = make_float2(ex2(av * dsum), hv);
-                }
-            }
-        }
+        if (LBK && OUTY && (hd.z & kWsFirst)) release_leaving(a, it, lane);
+        // ---- item end (aggregate pass): publish the chunk's (Π Ā, h_end from zero)
+        if (AG && (hd.z & kWsLast)) publish_pair<SPT, NQ>(a, it, d, live, g, lane, A2, dsum, h);
         if (!AG && (hd.z & kWsLast)) {
             // ---- item end: hand the state on, or write the final state
             float *dst = nullptr;
@@ -1073,6 +1246,69 @@ scan_ws_kernel(const __grid_constant__ Maps maps, const ScanArgs a) {
     }
     if (failed) record_error(a.status, 4 /* SSM_ERR_TIMEOUT */);
     if (OUTY && lane == 0) bulk_wait0();
+    return !failed;
+}
+
+// Each pair's eight barriers, set up by its consumer's lane 0 (again: after a
+// pass, with nothing pending on them).
+template <typename T>
+__device__ __forceinline__ void ws_init_bars(bool again) {
+    using S = WsTile<T>;
+    extern __shared__ __align__(128) unsigned char smem_all[];
+    const int warp = threadIdx.x >> 5;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem_all + (warp % S::PAIRS) * S::PIPE + S::off_bar);
+    if (warp / S::PAIRS == 0 && (threadIdx.x & 31) == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (again) mbar_inval(&bar[i]);
+            mbar_init(&bar[i], i < 2 ? 1 : kWsArrivals);
+        }
+        fence_mbar_init();
+    }
+}
+
+template <typename T, bool HAS_Z, bool ZOH, int WM>
+__global__ void __launch_bounds__(256, 2)
+scan_ws_kernel(const __grid_constant__ Maps maps, const __grid_constant__ ScanArgs a) {
+    ws_init_bars<T>(false);
+    __syncthreads();
+    (void)ws_pass<T, HAS_Z, ZOH, WM, false>(maps, a);
+}
+
+// The look-back launch of the warp-specialised scan: every pair runs
+// aggregate items until they run out, then main items.  Between the passes
+// the pair's two warps meet on a named barrier (one per pair; barrier 0 is
+// the block's), and unless a wait of either ran out, the consumer sets the
+// pair's barriers up afresh before they meet again.  The warps tell each
+// other how their pass ended in the second header slot, which the consumer
+// never reads during a pass.
+template <typename T, bool HAS_Z, bool ZOH>
+__global__ void __launch_bounds__(256, 2)
+scan_ws_lb_kernel(const __grid_constant__ Maps maps, const __grid_constant__ ScanArgs a) {
+    using S = WsTile<T>;
+    extern __shared__ __align__(128) unsigned char smem_all[];
+    ws_init_bars<T>(false);
+    __syncthreads();
+    const bool ok = ws_pass<T, false, ZOH, 1, true>(maps, a);
+    const int warp = threadIdx.x >> 5, pair = warp % S::PAIRS, role = warp / S::PAIRS;
+    volatile int *ended = reinterpret_cast<volatile int *>(smem_all + pair * S::PIPE + S::off_hdr + 16);
+    // immediate barrier ids, so that the block reserves five barriers, not all sixteen
+    static_assert(S::PAIRS == 4, "one named barrier per pair");
+    auto pair_sync = [&]() {
+        switch (pair) {
+            case 0: asm volatile("bar.sync 1, 64;" ::: "memory"); break;
+            case 1: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
+            case 2: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
+            default: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
+        }
+    };
+    if ((threadIdx.x & 31) == 0) ended[role] = ok ? 1 : 0;
+    pair_sync();
+    const bool both = ended[0] && ended[1];  // read before the next pass rewrites the slot
+    if (!both) return;
+    ws_init_bars<T>(true);
+    pair_sync();
+    (void)ws_pass<T, HAS_Z, ZOH, 0, true>(maps, a);
 }
 
 // B and C, [b][N][L] in the I/O type, widened once per launch to fp32
@@ -1096,40 +1332,6 @@ __global__ void __launch_bounds__(256) widen_bc_kernel(const ScanArgs a) {
         const int m = i / (32 * np), tt = (i / np) % 32, n = i % np, t = t0 + tt;
         if (t < L && in_range(((int64_t)b * L + t) * np + n, 1, (int64_t)a.batch * L * np))
             (m ? a.Ct : a.Bt)[((size_t)b * L + t) * np + n] = tile[m][n][tt];
-    }
-}
-
-// Chains the chunk aggregates from h0 (two-pass mode): carry[0] = h0 and
-// carry[k+1] = P_k · carry[k] + S_k, the state chunk k+1 starts from.
-// One thread per (b, d, n).  The aggregates do not depend on the chain, so they
-// are read kCarryBatch at a time before the chain steps through them: one L2
-// round trip per batch instead of one per chunk.
-constexpr int kCarryBatch = 16;
-__global__ void carry_kernel(const ScanArgs a) {
-    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const size_t total = (size_t)a.batch * a.dim * a.dstate;
-    if (i >= total) return;
-    const size_t N = (size_t)a.dstate;
-    const size_t bd = i / N;
-    const int n = (int)(i % N);
-    const int K = a.nchunks;
-    const float2 *__restrict__ agg = a.agg + bd * (K - 1) * N + n;
-    if (!in_range((int64_t)(bd * K * N + n), (int64_t)(K - 1) * N + 1, (int64_t)total * K)) return;
-    float *__restrict__ carry = a.carry + bd * K * N + n;
-    float h = a.h0 ? a.h0[i] : 0.f;
-    carry[0] = h;
-    for (int k0 = 0; k0 + 1 < K; k0 += kCarryBatch) {
-        float2 ps[kCarryBatch];
-#pragma unroll
-        for (int j = 0; j < kCarryBatch; ++j)
-            ps[j] = (k0 + j + 1 < K) ? agg[(size_t)(k0 + j) * N] : make_float2(1.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < kCarryBatch; ++j) {
-            if (k0 + j + 1 < K) {
-                h = fmaf(ps[j].x, h, ps[j].y);
-                carry[(size_t)(k0 + j + 1) * N] = h;
-            }
-        }
     }
 }
 
@@ -1178,10 +1380,11 @@ Split split_for(int64_t dstate) {
     return SSM_SCAN_N16_LANES == 1 ? Split{16, 1} : Split{8, 2};
 }
 
-template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, int MODE, bool ZOH>
+// LB: the look-back kernel, else the plain one.
+template <typename T, int SPT, int NG, bool HAS_Z, bool TMA, bool LB, bool ZOH>
 cudaError_t launch_one(const Maps &maps, const ScanArgs &a, int items, cudaStream_t st) {
     using S = WTile<T, SPT, NG>;
-    auto kern = scan_kernel<T, SPT, NG, HAS_Z, TMA, MODE, ZOH>;
+    auto kern = LB ? scan_lb_kernel<T, SPT, NG, HAS_Z, TMA, ZOH> : scan_kernel<T, SPT, NG, HAS_Z, TMA, ZOH>;
     static PerDevice resident;  // resident warps per SM for this instantiation
     int per_sm = 0;
     cudaError_t e = resident.get(
@@ -1200,10 +1403,11 @@ cudaError_t launch_one(const Maps &maps, const ScanArgs &a, int items, cudaStrea
     return cudaGetLastError();
 }
 
+// WM < 0: the look-back kernel; else scan_ws_kernel's pass WM.
 template <typename T, bool HAS_Z, bool ZOH, int WM = 0>
 cudaError_t launch_ws(const Maps &maps, const ScanArgs &a, int items, cudaStream_t st) {
     using S = WsTile<T>;
-    auto kern = scan_ws_kernel<T, HAS_Z, ZOH, WM>;
+    auto kern = WM < 0 ? scan_ws_lb_kernel<T, HAS_Z, ZOH> : scan_ws_kernel<T, HAS_Z, ZOH, (WM < 0 ? 0 : WM)>;
     static PerDevice resident;  // resident CTAs (four consumer warps each) per SM
     int per_sm = 0;
     cudaError_t e = resident.get(
@@ -1231,17 +1435,14 @@ cudaError_t launch_all(const Maps &maps, const ScanArgs &a, cudaStream_t st) {
     // bf16 I/O, first order: the warp-specialised form keeps eight consumer
     // warps per SM within 128 registers and 26 KB of shared memory per CTA.
     constexpr bool ws = SSM_SCAN_WS && TMA && SPT == 8 && NG == 2 && sizeof(T) == 2 && !ZOH;
-    if (a.nchunks > 1 && !a.chained) {
-        if constexpr (ws) e = launch_ws<T, false, ZOH, 1>(maps, a, a.groups * (a.nchunks - 1), st);
-        else e = launch_one<T, SPT, NG, false, TMA, 1, ZOH>(maps, a, a.groups * (a.nchunks - 1), st);
-        if (e != cudaSuccess) return e;
-        const size_t total = (size_t)a.batch * a.dim * a.dstate;
-        carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(a);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    if constexpr (ws) return launch_ws<T, HAS_Z, ZOH>(maps, a, a.groups * a.nchunks, st);
-    return launch_one<T, SPT, NG, HAS_Z, TMA, 0, ZOH>(maps, a, a.groups * a.nchunks, st);
+    // Chunks that run at once (K > 1, not chained) carry their start states by
+    // look-back inside the one launch, which holds every aggregate item of
+    // chunks 0 .. K-2 and then every main item.
+    const bool lb = a.nchunks > 1 && !a.chained;
+    const int items = a.groups * a.nchunks;
+    if constexpr (ws) return lb ? launch_ws<T, HAS_Z, ZOH, -1>(maps, a, items, st) : launch_ws<T, HAS_Z, ZOH, 0>(maps, a, items, st);
+    return lb ? launch_one<T, SPT, NG, HAS_Z, TMA, true, ZOH>(maps, a, items, st)
+              : launch_one<T, SPT, NG, HAS_Z, TMA, false, ZOH>(maps, a, items, st);
 }
 
 template <typename T, int SPT, int NG, bool ZOH>
@@ -1272,6 +1473,9 @@ cudaError_t dispatch_split(const Maps &maps, const ScanArgs &a, Split sp, bool t
 
 }  // namespace
 
+// Look-back terms of the chunk-length model below, µs.
+constexpr double kLookBackPerChunk = 1.1, kLookBackFixed = 8.0;
+
 int scan_groups(int64_t dstate) { return dstate <= 4 ? 1 : (dstate <= 8 ? 2 : 4); }
 
 ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t requested) {
@@ -1282,25 +1486,24 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
     p.groups = batch * ((dim + p.cpw - 1) / p.cpw);
     const int64_t resident = (int64_t)kSMs * kWarpsPerSM;
     const int64_t Lr = ((seqlen + 63) / 64) * 64;
-    // Chained when the groups alone fill the resident warps (a two-pass split
-    // would add an aggregate pass for parallelism the GPU does not need).
+    // Chained when the groups alone fill the resident warps (a look-back split
+    // would add aggregate items for parallelism the GPU does not need).
     p.chained = p.groups * 4 >= resident * 3;
     if (p.chained) {
         p.chunk_len = requested > 0 ? std::min<int64_t>(requested, Lr) : std::min<int64_t>(kDefaultChunk, Lr);
     } else if (requested > 0) {
         p.chunk_len = std::min<int64_t>(requested, Lr);
     } else {
-        // Two-pass: pick the chunk length with the least modelled time, in µs,
-        //   throughput:   all token-items of both passes (the aggregate pass
-        //                 costs ≈0.7 of the main one) spread over the resident
+        // Look-back: pick the chunk length with the least modelled time, in µs,
+        //   throughput:   all token-items of both kinds (an aggregate item
+        //                 costs ≈0.7 of a main one) spread over the resident
         //                 warps, ≈0.1 µs per token per warp when they are all busy;
-        //   critical path: one chunk walked by one warp in both passes, ≈0.07 µs
-        //                 per token when few warps share an SM;
-        //   carry:        the carry pass steps through the K chunks, ≈1.1 µs each,
-        //                 and the two extra launches (≈8 µs).
+        //   critical path: one chunk walked by one warp as both kinds of item,
+        //                 ≈0.07 µs per token when few warps share an SM;
+        //   look-back:    per chunk and in all (kLookBackPerChunk, kLookBackFixed).
         // The constants are fits to B300 timings of the 2 × 1536 × 16 × 2048 and
         // 1 × 5120 × 16 × 131072 layers over chunk lengths 64 .. 8192.  A single
-        // chunk (no aggregate pass) is one of the candidates.
+        // chunk (no aggregate items) is one of the candidates.
         double best = 1e300;
         p.chunk_len = Lr;
         for (int64_t len = Lr; len >= 64; len -= 64) {
@@ -1308,7 +1511,7 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
             if (K > 64) break;
             const double items = (double)p.groups * ((double)K + 0.7 * (double)(K - 1)) * (double)len;
             const double t = items * 0.1 / (double)resident + 1.7 * (double)len * 0.07 +
-                             (K > 1 ? 1.1 * (double)K + 8.0 : 0.0);
+                             (K > 1 ? kLookBackPerChunk * (double)K + kLookBackFixed : 0.0);
             if (t < best * 0.999) {
                 best = t;
                 p.chunk_len = len;

@@ -53,8 +53,9 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_params *p, ssm_stream_
     if (!scratch) return SSM_ERR_CUDA;
     q.workspace = scratch;
     q.workspace_bytes = SSM_NOALLOC_SCRATCH_BYTES;
-    // ssm_scan_fwd clears the status word at the head of the scratch before
-    // its launches; the chunk aggregates and carried states that follow are
-    // written in full before they are read, so stale contents do no harm.
+    // ssm_scan_fwd clears the status word and the chunk flags at the head of
+    // the scratch before its launches; the chunk pairs and carried states that
+    // follow are written before a flag says they are out, so stale contents do
+    // no harm.
     return ssm_scan_fwd(&q, stream);
 }

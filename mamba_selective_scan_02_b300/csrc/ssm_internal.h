@@ -68,15 +68,17 @@ struct ScanArgs {
     const float *h0;
     void *y;
     float *hL;
-    float2 *agg;     // two-pass mode: [b][D][K-1][N] (Π Ā, h_end from zero) per chunk
-    float *carry;    // two-pass: [b][D][K][N] state entering chunk k; chained: [b][D][N] hand-off
+    float2 *agg;     // look-back: [b][D][K-1][N] (Π Ā, h_end from zero) per chunk
+    float *carry;    // look-back: [b][D][K][N], slot k + 1 the state leaving chunk k;
+                     // chained: [b][D][N] hand-off
     int *status;     // device status word (0 = ok)
-    int *tickets;    // two work counters (main pass, aggregate pass), zero at launch
-    int *flags;      // chained mode: chunks finished per channel group, zero at launch
+    int *tickets;    // two work counters (main items, aggregate items), zero at launch
+    int *flags;      // chained: chunks finished per channel group; look-back: per
+                     // (group, chunk) 0 / 1 pair out / 2 leaving state out; zero at launch
     int chunk_len;   // tokens per chunk (multiple of 64)
     int nchunks;     // K
     int groups;      // channel groups: batch × ceil(dim / channels per warp)
-    int chained;     // 1: chunk k waits for chunk k-1's state; 0: two-pass carries
+    int chained;     // 1: chunk k waits for chunk k-1's state; 0 with K > 1: look-back
     float *Bt, *Ct;  // B and C widened to fp32, token-major: [b][L][np], zero beyond N
     int np;          // states per token row of Bt / Ct (N rounded up to 4, 8 or 16)
     float *ckpt;     // checkpoint launch only: the state at every 16-token tile start,
@@ -86,8 +88,9 @@ struct ScanArgs {
 // How a scan is cut into work items.  One warp owns a group of channels for
 // one chunk of the sequence.  Chained: the chunks of a group run in order,
 // each taking the previous one's final state (enough groups to fill the GPU).
-// Two-pass: an aggregate pass and a carry pass precompute every chunk's
-// starting state so that all chunks run at once (few groups, long sequences).
+// Look-back: every chunk first computes its pair from a zero state, so that
+// all chunks run at once and each finds its starting state by composing its
+// predecessors' pairs (few groups, long sequences); one launch either way.
 struct ScanPlan {
     int np;             // B / C row length after widening (N rounded up to 4, 8 or 16)
     int cpw;            // channels per warp

@@ -36,10 +36,10 @@ def _scan_inputs(g, b, D, N, L, dtype):
 
 
 # (name, batch, dim, dstate, seqlen, dtype, chunk_len): the fp32 kernel, the
-# warp-specialised bf16 kernel with a chained plan and with a two-pass plan
+# warp-specialised bf16 kernel with a chained plan and with a look-back plan
 SCANS = [("scan_f32", 2, 24, 5, 173, torch.float32, 0),
          ("scan_bf16_chained", 2, 1200, 16, 300, torch.bfloat16, 64),
-         ("scan_bf16_two_pass", 1, 32, 16, 700, torch.bfloat16, 64)]
+         ("scan_bf16_look_back", 1, 32, 16, 700, torch.bfloat16, 64)]
 STEPS = [("step_general", 3, 37, 5, torch.float32), ("step_16", 2, 96, 16, torch.bfloat16),
          ("step_stream", 2, 256, 16, torch.bfloat16)]
 CONVS = [("conv_rows", 2, 24, 203, 4, torch.bfloat16), ("conv_stream", 2, 40, 512, 4, torch.bfloat16)]

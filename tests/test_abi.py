@@ -98,11 +98,12 @@ def _bc_bytes(b, L, np_):
 def test_workspace_size():
     p = valid_scan(chunk_len=256)
     assert capi.ssm_scan_workspace_size(p) == 256 + _bc_bytes(2, 256, 16)   # one chunk
-    p = valid_scan(chunk_len=64)                             # 4 chunks of 64 tokens, two-pass
+    p = valid_scan(chunk_len=64)                             # 4 chunks of 64 tokens, look-back
     bdn = 2 * 64 * 16
+    flags = -(-(2 * 64 // 16) * 4 * 4 // 256) * 256           # one per (group of 16 channels, chunk)
     agg = -(-bdn * 3 * 8 // 256) * 256
     carry = -(-bdn * 4 * 4 // 256) * 256
-    assert capi.ssm_scan_workspace_size(p) == 256 + agg + carry + _bc_bytes(2, 256, 16)
+    assert capi.ssm_scan_workspace_size(p) == 256 + flags + agg + carry + _bc_bytes(2, 256, 16)
     # the small-model layer shape is split into chunks automatically
     p = valid_scan(batch=2, dim=1536, seqlen=2048)
     assert capi.ssm_scan_workspace_size(p) > 256 + _bc_bytes(2, 2048, 16)
@@ -297,7 +298,7 @@ def test_bwd_workspace_size_with_forward_checkpoints():
     # TMA cannot describe
     assert capi.ssm_scan_bwd_workspace_size(valid_bwd(batch=b, dim=d, seqlen=L, zoh=1)) == base
     assert capi.ssm_scan_bwd_workspace_size(valid_bwd(batch=b, dim=d, seqlen=L, io_dtype=capi.SSM_F32)) == base
-    small = valid_bwd(batch=1, dim=d, seqlen=L)                # 320 groups: a two-pass forward plan
+    small = valid_bwd(batch=1, dim=d, seqlen=L)                # 320 groups: a look-back forward plan
     g1 = d // 16
     assert capi.ssm_scan_bwd_workspace_size(small) == (
         256 + 2 * (-(-g1 * 4 // 256) * 256) + 2 * (-(-d * n * 4 // 256) * 256) + g1 * ntiles * 1024)

@@ -41,7 +41,7 @@ def test_tiny_fp32_workload():
     (2, 40, 16, 200, torch.bfloat16, {}),                 # TMA path, ragged channel tile and last tile
     (1, 33, 5, 203, torch.bfloat16, {}),                  # row pitch not 16-B aligned: plain loads
     (2, 7, 3, 97, torch.float32, {}),
-    (1, 300, 8, 128, torch.float32, dict(chunk_len=64)),  # two chunks joined by a carried state
+    (1, 300, 8, 128, torch.float32, dict(chunk_len=64)),  # two chunks joined by look-back
     (2, 64, 16, 1000, torch.bfloat16, dict(chunk_len=128, h0=True)),
     (1, 16, 1, 1, torch.float32, {}),                     # L = 1, N = 1
     (3, 130, 12, 257, torch.bfloat16, dict(z=False)),     # padded state group, no gate

@@ -28,7 +28,7 @@ def _case(b, D, N, L, dtype, seed, h0=True):
 
 @pytest.mark.parametrize("b,D,N,L,dtype,chunk", [
     (1, 40, 16, 200, torch.float32, 0),
-    (2, 64, 16, 512, torch.bfloat16, 128),      # two-pass chunks
+    (2, 64, 16, 512, torch.bfloat16, 128),      # look-back chunks
     (1, 33, 5, 203, torch.float32, 0),          # plain loads, small N
     (4, 3600, 16, 512, torch.bfloat16, 64),     # chained chunks, partial last group
 ])

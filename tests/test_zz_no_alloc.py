@@ -4,9 +4,9 @@ device memory (its chunk scratch is a fixed array inside the library).
 It runs the same kernels as ssm_scan_fwd on the same inputs, so its output must
 equal ssm_scan_fwd's bit for bit, call after call.  The shared scratch keeps
 the previous call's contents — chained plans keep their hand-off flags and
-states there, two-pass plans their chunk aggregates — so each case runs
-several calls in a row on different inputs: two chained layers, then a
-two-pass one, then a chained one again.  One of them is also checked against
+states there, look-back plans their chunk flags, pairs and carried states —
+so each case runs several calls in a row on different inputs: two chained
+layers, then a look-back one, then a chained one again.  One of them is also checked against
 the oracle.  This file is collected last so that a run stopping at its first
 failure has already run every other test.
 """
@@ -21,9 +21,9 @@ from ssm_testutil import assert_close, oracle_scan_sampled, sample_channels
 pytestmark = pytest.mark.gpu
 
 # A layer whose default plan is chained (enough channel groups to fill the GPU)
-# and one whose plan is two-pass (few groups, the sequence cut into chunks).
+# and one whose plan is look-back (few groups, the sequence cut into chunks).
 CHAINED = dict(b=4, D=5000, N=16, L=512)
-TWO_PASS = dict(b=2, D=96, N=16, L=1000)
+LOOK_BACK = dict(b=2, D=96, N=16, L=1000)
 
 
 def _inputs(seed, b, D, N, L, dtype=torch.bfloat16):
@@ -74,7 +74,7 @@ def _check_equal(inp, chunk_len, what):
 
 @pytest.mark.parametrize("chunk_len", [0, 64])
 def test_no_alloc_equals_workspace_entry_point_call_after_call(chunk_len):
-    calls = [(CHAINED, 21), (CHAINED, 22), (TWO_PASS, 23), (CHAINED, 24)]
+    calls = [(CHAINED, 21), (CHAINED, 22), (LOOK_BACK, 23), (CHAINED, 24)]
     kinds = []
     for n, (shape, seed) in enumerate(calls):
         inp = _inputs(seed, **shape)
