@@ -257,18 +257,24 @@ bwd_ckpt_kernel(const BwdArgs a) {
 }
 
 // ------------------------------------------------------------------ pass 2
+// The tile's outputs du, dΔraw and dz go into the slots of Gp, Sg and Sp: the
+// adjoint step of token t has the channel's first lane read those three terms
+// (the only lane that needs them) and then overwrite them, so no other lane
+// reads a slot it writes.  One row of channel sums serves dC (flushed before
+// the walk) and then dB.  27.1 KB a warp with two lanes per channel, so that
+// eight warps fit on an SM instead of seven.
 template <int NG> struct RevSmem {
     static constexpr int CPW = BwdShape<NG>::CPW, NP = BwdShape<NG>::NP;
     float4 Hs[TS * 2 * 32];                 // state after token t: [t][half][lane]
     float Bs[TS * NP], Cs[TS * NP];         // fp32 token-major rows
-    float acc[TS * 2 * NP];                 // [t][dB | dC][n]: the tile's channel sums
+    float acc[TS * NP];                     // [t][n]: the tile's channel sums, dC then dB
     float Dl[CPW * TSP], Du[CPW * TSP], U[CPW * TSP], Sg[CPW * TSP], Yh[CPW * TSP], Gp[CPW * TSP],
-        Sp[CPW * TSP];                      // per-channel token terms
-    float Odu[CPW * TSP], Odd[CPW * TSP], Odz[CPW * TSP];  // outputs of the tile
+        Sp[CPW * TSP];                      // per-channel token terms; Gp, Sg, Sp then du, dΔraw, dz
 };
+static_assert(TS == 16, "the channel-sum flush maps 16 tokens onto half a warp");
 
 template <typename T, int NG, bool HAS_Z, bool ZOH, bool VEC>
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(32, kBwdWarpsPerSM)
 bwd_rev_kernel(const BwdArgs a) {
     using S = BwdShape<NG>;
     constexpr int CPW = S::CPW, NP = S::NP, OWN = S::OWN, NQ = SPT / 2;
@@ -471,10 +477,26 @@ bwd_rev_kernel(const BwdArgs a) {
                     }
                 }
 #pragma unroll
-                for (int j = 0; j < HN; ++j) sm.acc[(t * 2 + m) * NP + HN * hh + j] = acc[j];
+                for (int j = 0; j < HN; ++j) sm.acc[t * NP + HN * hh + j] = acc[j];
+                (void)m;
+            };
+            // the sums into memory (lane: one token, half of the states)
+            auto flush_sums = [&](float *base) {
+                constexpr int HN = NP / 2;
+                const int t = lane & 15, hh = lane >> 4;
+                if (t0 + t < L && in_range((int64_t)it.b * N * L + t0 + t, (int64_t)(N - 1) * L + 1, (int64_t)a.batch * N * L)) {
+                    float *dst = base + (size_t)it.b * N * L + t0 + t;
+#pragma unroll
+                    for (int j = 0; j < HN; ++j) {
+                        const int n = HN * hh + j;
+                        if (n < N) atomicAdd(dst + (size_t)n * L, sm.acc[t * NP + n]);
+                    }
+                }
             };
             // dC = Σ_c ŷ·h from the recomputed states
             channel_sum(1, true);
+            __syncwarp();
+            flush_sums(a.dC);
 
             // ---- the adjoint, backwards through the tile
             float2 hcur[NQ];
@@ -543,13 +565,15 @@ bwd_rev_kernel(const BwdArgs a) {
                     if (ZOH) sab += __shfl_xor_sync(FULL, sab, 1);
                 }
                 const float dut = fmaf(yh, skip, dl * slb);
-                const float ddr = (ZOH ? fmaf(uu, sab, saa) : fmaf(uu, slb, saa)) * sm.Sg[e];
+                // the first lane's alone (dΔraw out, Σ for dbias); the other lane reads no Sg
+                const float ddr = g == 0 ? (ZOH ? fmaf(uu, sab, saa) : fmaf(uu, slb, saa)) * sm.Sg[e] : 0.f;
                 dD_acc = fmaf(yh, uu, dD_acc);
                 db_acc += ddr;
                 if (g == 0) {
-                    sm.Odu[e] = dut;
-                    sm.Odd[e] = ddr;
-                    if (HAS_Z) sm.Odz[e] = sm.Gp[e] * sm.Sp[e];
+                    const float dzt = HAS_Z ? sm.Gp[e] * sm.Sp[e] : 0.f;
+                    sm.Gp[e] = dut;
+                    sm.Sg[e] = ddr;
+                    if (HAS_Z) sm.Sp[e] = dzt;
                 }
                 // the lane's dB partials replace the state after token t, which
                 // the walk no longer needs (token t+1 read it as its h_{t−1})
@@ -563,15 +587,8 @@ bwd_rev_kernel(const BwdArgs a) {
             channel_sum(0, false);
             __syncwarp();
 
-            // ---- the tile's dB, dC channel sums into memory (lane: one token,
-            // one of dB / dC, every state); du, dΔraw, dz out
-            {
-                const int t = lane & 15, m = lane >> 4;
-                if (t0 + t < L && in_range((int64_t)it.b * N * L + t0 + t, (int64_t)(N - 1) * L + 1, (int64_t)a.batch * N * L)) {
-                    float *dst = (m ? a.dC : a.dB) + (size_t)it.b * N * L + t0 + t;
-                    for (int n = 0; n < N; ++n) atomicAdd(dst + (size_t)n * L, sm.acc[(t * 2 + m) * NP + n]);
-                }
-            }
+            // ---- the tile's dB sums into memory; du, dΔraw, dz out
+            flush_sums(a.dB);
             if (live) {
                 T *gdu = static_cast<T *>(a.du) + rowoff, *gdd = static_cast<T *>(a.ddelta) + rowoff;
                 T *gdz = HAS_Z && a.dz ? static_cast<T *>(a.dz) + rowoff : nullptr;
@@ -579,9 +596,9 @@ bwd_rev_kernel(const BwdArgs a) {
                 for (int i = 0; i < OWN; ++i) {
                     const int j = OWN * g + i, t = t0 + j;
                     if (t < L && in_range((int64_t)rowoff + t, 1, (int64_t)a.batch * D * L)) {
-                        gdu[t] = IO<T>::from_f(sm.Odu[c * TSP + j]);
-                        gdd[t] = IO<T>::from_f(sm.Odd[c * TSP + j]);
-                        if (gdz) gdz[t] = IO<T>::from_f(sm.Odz[c * TSP + j]);
+                        gdu[t] = IO<T>::from_f(sm.Gp[c * TSP + j]);
+                        gdd[t] = IO<T>::from_f(sm.Sg[c * TSP + j]);
+                        if (gdz) gdz[t] = IO<T>::from_f(sm.Sp[c * TSP + j]);
                     }
                 }
             }
