@@ -34,7 +34,7 @@ def _al(n):
     return -(-n // 256) * 256
 
 
-def _inputs(b, D, N, L, dtype, seed, zoh_safe=False):
+def _inputs(b, D, N, L, dtype, seed, zoh_safe=False, gate=True, init=True):
     g = torch.Generator().manual_seed(seed)
 
     def rn(*s, std=1.0):
@@ -42,14 +42,14 @@ def _inputs(b, D, N, L, dtype, seed, zoh_safe=False):
     A = -torch.rand(D, N, generator=g).add_(0.5)
     if zoh_safe:
         A = A - 0.1
-    return dict(u=rn(b, D, L), delta=rn(b, D, L, std=0.5), z=rn(b, D, L), B=rn(b, N, L), C=rn(b, N, L),
-                A=A, Dskip=torch.randn(D, generator=g),
+    return dict(u=rn(b, D, L), delta=rn(b, D, L, std=0.5), z=rn(b, D, L) if gate else None, B=rn(b, N, L),
+                C=rn(b, N, L), A=A, Dskip=torch.randn(D, generator=g),
                 bias=torch.log(torch.expm1(torch.empty(D).uniform_(1e-3, 1e-1, generator=g))).float(),
-                h0=torch.randn(b, D, N, generator=g) * 0.5)
+                h0=torch.randn(b, D, N, generator=g) * 0.5 if init else None)
 
 
 def _run(inp, chunk_len, zoh=False):
-    d = {k: v.cuda().contiguous() for k, v in inp.items()}
+    d = {k: (v.cuda().contiguous() if v is not None else None) for k, v in inp.items()}
     b, D, L = d["u"].shape
     N = d["B"].shape[1]
     y = torch.empty_like(d["u"])
@@ -65,8 +65,12 @@ def _run(inp, chunk_len, zoh=False):
     return y, hL, ws.cpu().numpy(), plan
 
 
-# (b, D, N, L, dtype, chunk_len, zoh): each a look-back plan of a different kernel
+# (b, D, N, L, dtype, chunk_len, zoh[, gate, h0]): each a look-back plan of a
+# different kernel or edge
 CASES = [
+    (1, 20, 16, 641, torch.bfloat16, 64, False, False, False),  # plain loads, last chunk one token, no z, no h0
+    (1, 20, 16, 648, torch.bfloat16, 64, False, False, False),  # warp-specialised, last chunk one 8-token tile
+    (2, 8, 5, 129, torch.float32, 64, False, True, False),      # fp32, last chunk one token, h0 = 0
     (1, 32, 16, 700, torch.bfloat16, 64, False),     # warp-specialised, 11 chunks, ragged last chunk
     (2, 48, 16, 4096, torch.bfloat16, 64, False),    # warp-specialised, 64 chunks (the most the plan cuts)
     (2, 24, 5, 173, torch.float32, 64, False),       # fp32, 8 states per lane
@@ -77,9 +81,11 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("b,D,N,L,dtype,chunk,zoh", CASES)
-def test_carried_states_are_the_sequential_chain(b, D, N, L, dtype, chunk, zoh):
-    inp = _inputs(b, D, N, L, dtype, seed=b * 7 + D + N + L, zoh_safe=zoh)
+@pytest.mark.parametrize("case", CASES)
+def test_carried_states_are_the_sequential_chain(case):
+    b, D, N, L, dtype, chunk, zoh = case[:7]
+    gate, init = case[7:9] if len(case) > 7 else (True, True)
+    inp = _inputs(b, D, N, L, dtype, seed=b * 7 + D + N + L, zoh_safe=zoh, gate=gate, init=init)
     y, hL, ws, plan = _run(inp, chunk, zoh)
     K, G = plan["nchunks"], plan["groups"]
     assert not plan["chained"] and K == -(-L // chunk) and K > 1
@@ -95,7 +101,7 @@ def test_carried_states_are_the_sequential_chain(b, D, N, L, dtype, chunk, zoh):
     # floats is exact in fp64 and the sum is rounded once there, then to fp32: the
     # same value as the fp32 fma unless the fp64 sum lands on an fp32 rounding
     # midpoint, which these few thousand steps do not.
-    h = inp["h0"].numpy().astype(np.float32)
+    h = (inp["h0"] if inp["h0"] is not None else torch.zeros(b, D, N)).numpy().astype(np.float32)
     for k in range(K - 1):
         P, S = agg[:, :, k, :, 0], agg[:, :, k, :, 1]
         assert np.isfinite(P).all() and np.isfinite(S).all() and (P >= 0).all() and (P <= 1).all()
